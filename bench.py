@@ -1,0 +1,358 @@
+"""Throughput of the SANA-Video linear-attention layer core on GB300.
+
+One step = one layer call (per-split KV partial sums, fixed-order reduction, apply +
+normalise) over a whole synthetic layer of the 720p/193-frame profile (H=20,
+N=180320, D=112, 'high' tier, FP32 output) unless --workload/--mode say otherwise.
+
+Prints ONE JSON line (rank 0):
+  value      tokens/s per layer call, inputs resident in HBM (device-timed, CUDA events)
+  e2e        the same metric through the C ABI's host-buffer call (pinned host memory;
+             host->device copies of q/k/v/den and the device->host copy of out are inside)
+  roofline   the dominant kernel's algorithmic bytes / its mean event-timed duration
+             against the measured HBM copy bandwidth
+  cpu_baseline  the FP64 oracle on the host cores on a bounded sample of the same layer
+
+--impl reference times the FP64 CPU oracle as it stands (the pages publish no runnable
+implementation of this path); under torchrun only rank 0 runs it.
+With --gpus N > 1 (torchrun, one process per GPU) every rank runs an independent replica
+of the layer: the layer has no cross-GPU exchange here, so the scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "linear-attn tokens/s per layer; achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algorithmic_bytes(H, N, D, out_bytes):
+    """Per layer call: read Q, K, V (BF16) and den (FP32) once, write out once."""
+    kv_partial = H * N * D * 2 * 2
+    apply = H * N * (D * 2 + 4 + D * out_bytes)
+    return {"kv_partial": kv_partial, "apply": apply, "total": kv_partial + apply}
+
+
+def algorithmic_flops(H, N, D):
+    return {"kv_partial": 2 * H * N * D * D, "apply": 2 * H * N * D * D}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu capture, or None when the kernel
+    source changed since the capture (or no capture exists)."""
+    p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get("kernels", {}).get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != ent["source_sha256"]:
+            return None
+    return ent.get("bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return world, rank, local, dist
+    return 1, 0, 0, None
+
+
+def barrier(dist, dev=None):
+    if dist is not None:
+        if dev is not None and dev.type == "cuda":
+            dist.barrier(device_ids=[dev.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value, dev):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample_time(layer_np, heads_sample, threads=None):
+    """Wall time of the oracle on the first `heads_sample` heads (all tokens)."""
+    import oracle
+    qb, kb, vb, den = layer_np
+    if threads:
+        oracle.set_num_threads(threads)
+    h = heads_sample
+    q, k, v, d = (np.ascontiguousarray(x[:h]) for x in (qb, kb, vb, den))
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, d)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(layer_np, H, N, budget_s=12.0):
+    """Oracle tokens/s per layer call, scaled from a sample of whole heads."""
+    import oracle
+    cores = oracle.num_threads()
+    t1 = oracle_sample_time(layer_np, 1)
+    hs = int(max(1, min(H, budget_s // max(t1, 1e-3))))
+    t = oracle_sample_time(layer_np, hs) if hs > 1 else t1
+    per_layer = t * H / hs
+    return {"value": N / per_layer, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{hs} of {H} heads, all {N} tokens (KV + apply, FP64); time scaled x{H / hs:.2f} "
+                      f"to one layer call ({t:.2f} s measured)"}
+
+
+def layer_to_numpy(layer):
+    import oracle
+    return oracle.torch_inputs_to_numpy(layer)
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, w, world, rank):
+    """The FP64 oracle as it stands, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    from video_diffusion_dit_gb300 import synth
+    # inputs of the same workload; each step runs the oracle on a bounded sample of heads
+    layer = synth.make_workload(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    layer_np = layer_to_numpy(layer)
+    del layer
+    import oracle
+    cores = oracle.num_threads()
+    t1 = oracle_sample_time(layer_np, 1)
+    step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    hs = int(max(1, min(w.heads, step_budget // max(t1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_time(layer_np, hs)
+    times = [oracle_sample_time(layer_np, hs) * w.heads / hs for _ in range(args.steps)]
+    per_layer = sum(times) / len(times)
+    value = w.tokens / per_layer
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} layer: H={w.heads}, N={w.tokens}, D={w.head_dim}", "mode": "exact (FP64)",
+                   "impl_detail": "FP64 CPU oracle (plain C, OpenMP over independent outputs)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {hs} of {w.heads} heads, all {w.tokens} tokens; time scaled "
+                                   f"x{w.heads / hs:.2f} to one layer call"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_ours(args, w, world, rank, local, dist):
+    from video_diffusion_dit_gb300 import lin_attn, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    H, N, D = w.heads, w.tokens, w.head_dim
+    out_dtype = torch.float32 if args.out_dtype == "f32" else torch.bfloat16
+    out_bytes = 4 if out_dtype == torch.float32 else 2
+    layer = synth.make_layer(H, N, D, w.seed + rank, w.grid, device=dev)
+    out = torch.empty(1, H, N, D, dtype=out_dtype, device=dev)
+    ctx = lin_attn.LinAttn(H, N, D, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ctx.forward(layer["q_rot"], layer["k_rot"], layer["v"], layer["den"], out=out, mode=args.mode, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if ctx.device_status() != 0:
+        raise RuntimeError("kernel status error during warm-up")
+
+    # ---- timed region: whole-layer throughput (CUDA events on the launching stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for row in ev:  # create the CUDA events before the timed region
+        for e in row:
+            e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            ctx.set_stage_events(ev[i])
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    elapsed_ms = max_over_ranks(dist, start.elapsed_time(end), dev)
+    if ctx.device_status() != 0:
+        raise RuntimeError("kernel status error in the timed region")
+    stage_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j, name in enumerate(("kv_partial", "kv_finalize", "apply"))}
+    ms_per_step = elapsed_ms / args.steps
+    value = world * N / (ms_per_step / 1e3)
+
+    # ---- end to end through the host-buffer entry point (pinned host memory)
+    host = {k: t.cpu().pin_memory() for k, t in layer.items()}
+    hout = torch.empty(1, H, N, D, dtype=out_dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode, stream=stream)
+    barrier(dist, dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
+                         stream=stream)
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev) / e2e_steps
+    h2d = 3 * H * N * D * 2 + H * N * 4
+    d2h = H * N * D * out_bytes
+
+    nbytes = algorithmic_bytes(H, N, D, out_bytes)
+    peak, peak_kind = load_peaks()
+    dom = max(("kv_partial", "apply"), key=lambda k: stage_ms[k])
+    achieved = nbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+    kernel_names = {"kv_partial": "kv_partial_tc_kernel" if args.mode == "high" else "kv_partial_ffma_kernel",
+                    "apply": "apply_tc_kernel" if args.mode == "high" else "apply_ffma_kernel"}
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(layer_to_numpy(layer), H, N, args.cpu_budget) if (world == 1 and not args.no_cpu) else None
+        clk = clocks.summary()
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": f"{w.name} layer: H={H}, N={N}, D={D}", "mode": args.mode, "out_dtype": args.out_dtype,
+                "accumulate": "f32", "l2": "inputs larger than L2 (no flush needed)",
+                "bytes_per_call": nbytes["total"], "parallelism": f"replicas x{world}",
+            },
+            "achieved_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
+            "stage_ms": stage_ms,
+            "roofline": {"kernel": kernel_names[dom], "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": kernel_traffic(kernel_names[dom]),
+                         "algorithmic_bytes": nbytes[dom]},
+            "e2e": {"value": world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+    ctx.close()
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="720p_193f")
+    ap.add_argument("--mode", default="high", choices=["high", "lossless"])
+    ap.add_argument("--out-dtype", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    from video_diffusion_dit_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    world, rank, local, dist = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, w, world, rank)
+    else:
+        res = run_ours(args, w, world, rank, local, dist)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * lin_attn.h - C ABI of the GB300 (sm_103a) SANA-Video linear-attention layer core.
+ *
+ * Operation (page "PR #35728 完整报告 - [diffusion] Accelerate SANA-Video linear
+ * attention in quality=high", section 关键源码片段, snippets
+ * `sana_video_linear_attention_site.py` (try_sana_video_linear_attention) and
+ * `sana_video.py` (SanaVideoLinearAttention.forward, FP32 fallback chain)):
+ * for every head h of a batch-1 layer,
+ *
+ *     KV[h]  = K_rot[h]^T . V[h]                 a D x D matrix, reduced over the N tokens
+ *     out[h] = (Q_rot[h] . KV[h]) / den[h]       den[h][n] is the layer's normaliser denominator
+ *
+ * The page keeps the operands as [B, H, D, N] views and forms scores = V . K_rot^T and
+ * (scores @ Q_rot) * normalizer; with contiguous [1, H, N, D] storage those are the
+ * transposes of the two products above, so the numbers are the same.
+ *
+ * Quality tiers (same page, 功能与动机 and the site snippet):
+ *   LIN_ATTN_MODE_HIGH      first GEMM on BF16 operands, FP32 accumulation and output;
+ *                           second GEMM at FP32 accuracy (here: Q . (KV_hi + KV_mid + KV_lo)
+ *                           with KV split into three BF16 terms, FP32 accumulation).
+ *   LIN_ATTN_MODE_LOSSLESS  Q, K, V upcast to FP32 before both GEMMs (FP32 FMA on CUDA cores).
+ * Both tiers have the same exact result; they differ only in rounding.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are contiguous row-major, batch 1.  q_rot, k_rot, v: BF16 [1, H, N, D];
+ *     normalizer: FP32 [1, H, N, 1] (the denominator, positive); out: FP32 or BF16 [1, H, N, D].
+ *   - Device pointers must live on the context's device and be 16-byte aligned.
+ *   - The caller owns every tensor; the context owns only its scratch.
+ *   - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream) and return
+ *     without synchronising, unless stated otherwise.
+ *   - A context may be used by one stream at a time (its scratch is shared by all calls).
+ *   - `out` must not overlap any input.
+ *   - Return value: LIN_ATTN_OK or one of the LIN_ATTN_ERR_* codes below; on error nothing
+ *     was enqueued (except LIN_ATTN_ERR_CUDA after a failed launch) and
+ *     lin_attn_last_error() gives a one-line reason for the calling thread.
+ *   - Results are deterministic: for the same inputs the output is bitwise the same from
+ *     run to run (the cross-CTA reduction has a fixed order that depends only on N, H, D).
+ */
+#ifndef LIN_ATTN_H
+#define LIN_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st * */
+struct CUevent_st;  /* cudaEvent_t  == struct CUevent_st *  */
+
+typedef struct lin_attn_ctx lin_attn_ctx;
+
+enum lin_attn_mode { LIN_ATTN_MODE_HIGH = 0, LIN_ATTN_MODE_LOSSLESS = 1 };
+enum lin_attn_out_dtype { LIN_ATTN_OUT_F32 = 0, LIN_ATTN_OUT_BF16 = 1 };
+
+enum lin_attn_status {
+    LIN_ATTN_OK = 0,
+    LIN_ATTN_ERR_INVALID_ARG = 1, /* null pointer, size out of range, bad enum value        */
+    LIN_ATTN_ERR_UNSUPPORTED = 2, /* head_dim not a multiple of 16 in [16, 128], no sm_100+ */
+    LIN_ATTN_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned                */
+    LIN_ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a kernel launch failed   */
+    LIN_ATTN_ERR_OOM = 5,         /* device or pinned-host allocation failed                */
+    LIN_ATTN_ERR_TIMEOUT = 6      /* a kernel gave up waiting on one of its own barriers    */
+};
+
+/*
+ * Create a context for layers of `heads` heads, up to `max_tokens` tokens and head dim
+ * `head_dim` on CUDA device `device`.  Allocates all scratch the forward pass needs
+ * (per-split partial KV sums, the reduced KV, its three-term BF16 image, a status word),
+ * so lin_attn_forward never allocates.  head_dim must be a multiple of 16 in [16, 128];
+ * smaller head dims are served by zero-padding D (padding leaves out[..., :D] unchanged).
+ * 1 <= heads <= 4096, 1 <= max_tokens <= 2^30.  On success *ctx is set; on failure *ctx
+ * is NULL.  The calling thread's current device is left as it was.
+ */
+int lin_attn_create(lin_attn_ctx **ctx, int heads, int64_t max_tokens, int head_dim, int device);
+
+/* Free the context and its scratch (waits for the device to finish with it).  NULL is OK. */
+int lin_attn_destroy(lin_attn_ctx *ctx);
+
+/*
+ * One layer call on device tensors (see the conventions above):
+ *   q_rot, k_rot, v : BF16 [1, heads, n_tokens, head_dim]
+ *   normalizer      : FP32 [1, heads, n_tokens, 1], the denominator den[h][n]
+ *   out             : out_dtype (LIN_ATTN_OUT_F32 / LIN_ATTN_OUT_BF16) [1, heads, n_tokens, head_dim];
+ *                     BF16 output is rounded to nearest-even from the FP32 result
+ *   n_tokens        : 1 <= n_tokens <= max_tokens of the context
+ *   mode            : LIN_ATTN_MODE_HIGH or LIN_ATTN_MODE_LOSSLESS
+ * Enqueues three kernels (per-split KV partial sums, fixed-order reduction, apply +
+ * normalise) on `stream`.
+ */
+int lin_attn_forward(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
+                     const float *normalizer, void *out, int out_dtype, int64_t n_tokens,
+                     int mode, struct CUstream_st *stream);
+
+/*
+ * Same layer call on HOST buffers (same shapes and dtypes, any alignment).  Copies the
+ * inputs to device staging owned by the context, runs the layer, copies the result
+ * back and synchronises `stream` before returning: when it returns OK, `out` holds the
+ * result.  The staging is allocated on the first call (LIN_ATTN_ERR_OOM if that fails)
+ * and kept until lin_attn_destroy.  Page-locked host buffers give full copy bandwidth;
+ * pageable ones work but copy slower.
+ */
+int lin_attn_forward_host(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
+                          const float *normalizer, void *out, int out_dtype, int64_t n_tokens,
+                          int mode, struct CUstream_st *stream);
+
+/*
+ * Test hook: enqueue a copy of the reduced KV of the last forward call, FP32
+ * [heads, head_dim, head_dim] row-major (KV[h][i][j] = sum_n K_rot[h][n][i] V[h][n][j]),
+ * into the device buffer kv_out.
+ */
+int lin_attn_debug_kv(lin_attn_ctx *ctx, float *kv_out, struct CUstream_st *stream);
+
+/*
+ * Synchronise `stream`, then return and clear the context's device status word:
+ * LIN_ATTN_OK, or LIN_ATTN_ERR_TIMEOUT if a kernel of an earlier call gave up waiting
+ * on one of its barriers (its output is then incomplete).
+ */
+int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
+
+/*
+ * Number of token splits per head used by the KV reduction for this shape (>= 1).  It
+ * depends on (heads, n_tokens, head_dim) only - never on the GPU - which is what makes
+ * the reduction order, and so the result, reproducible.  Returns -1 on bad arguments.
+ */
+int lin_attn_num_splits(int heads, int64_t n_tokens, int head_dim);
+
+/*
+ * Timing hook.  Arms `n_events` (must be 4) CUDA events (created with timing enabled)
+ * for the NEXT lin_attn_forward call only: events[0] is recorded before the KV partial
+ * kernel, events[1] after it, events[2] after the reduction, events[3] after apply.
+ * Passing n_events = 0 disarms.
+ */
+int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *events, int n_events);
+
+/* Static description of a status code. */
+const char *lin_attn_error_string(int status);
+
+/* One-line reason for the last error returned on the calling thread ("" if none). */
+const char *lin_attn_last_error(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int lin_attn_version(void);
+
+#define LIN_ATTN_VERSION 100
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* LIN_ATTN_H */

@@ -1,0 +1,124 @@
+"""The C-ABI library: it loads, exports every entry point the header declares, and its
+host-side argument checks answer without touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "lin_attn.h")
+LIB = os.path.join(ROOT, "video_diffusion_dit_gb300", "liblin_attn.so")
+
+
+@pytest.fixture(scope="module")
+def la():
+    if not os.path.exists(LIB):
+        from video_diffusion_dit_gb300 import build
+        build.build()
+    from video_diffusion_dit_gb300 import lin_attn
+    return lin_attn
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lin_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("lin_attn_create", "lin_attn_forward", "lin_attn_destroy"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(la):
+    lib = ctypes.CDLL(LIB)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in lin_attn.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(lin_attn_\w+)\b", out))
+    assert exported == set(declared_functions()), "exports and header declarations differ"
+    assert set(la.EXPORTS) == set(declared_functions())
+
+
+def test_header_compiles_as_c():
+    src = '#include "lin_attn.h"\nint main(void){ return lin_attn_version() == LIN_ATTN_VERSION ? 0 : 1; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-"], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_version_and_error_strings(la):
+    assert la.lib.lin_attn_version() == 100
+    for code in range(7):
+        assert la.error_string(code) and la.error_string(code) != "unknown status"
+    assert la.error_string(99) == "unknown status"
+
+
+def test_create_rejects_bad_arguments_before_any_cuda_call(la):
+    h = ctypes.c_void_p(1234)
+    assert la.lib.lin_attn_create(None, 20, 1000, 112, 0) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_create(ctypes.byref(h), 0, 1000, 112, 0) == la.ERR_INVALID_ARG
+    assert not h.value  # *ctx cleared on failure
+    assert la.lib.lin_attn_create(ctypes.byref(h), 20, 0, 112, 0) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_create(ctypes.byref(h), 20, (1 << 30) + 1, 112, 0) == la.ERR_INVALID_ARG
+    for d in (0, 8, 24, 100, 144):
+        assert la.lib.lin_attn_create(ctypes.byref(h), 20, 1000, d, 0) == la.ERR_UNSUPPORTED
+    assert b"head_dim" in la.lib.lin_attn_last_error()
+
+
+def test_calls_on_null_context_are_rejected(la):
+    p = ctypes.c_void_p(16)
+    assert la.lib.lin_attn_forward(None, p, p, p, p, p, 0, 10, 0, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_forward_host(None, p, p, p, p, p, 0, 10, 0, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_debug_kv(None, p, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_device_status(None, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_set_stage_events(None, None, 0) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_destroy(None) == la.OK
+
+
+def test_split_plan_depends_on_shape_only(la):
+    # The plan fixes the reduction order: it must be a pure function of (H, N, D),
+    # cover every token exactly once, and stay within the 64-split register budget.
+    for H in (1, 2, 12, 20, 32, 64):
+        for N in (1, 63, 64, 65, 256, 1000, 32760, 180320, 262144):
+            S = la.num_splits(H, N, 112)
+            assert 1 <= S <= 64
+            assert S == la.num_splits(H, N, 112) == la.num_splits(H, N, 64)
+            s0 = min(64, -(-760 // H))
+            chunk = -(-(-(-N // s0)) // 64) * 64
+            assert S == -(-N // chunk)
+            assert (S - 1) * chunk < N <= S * chunk
+    assert la.num_splits(20, 180320, 112) == 38
+    assert la.num_splits(20, 32760, 112) == 37
+    assert la.num_splits(0, 10, 112) == -1
+
+
+def test_binding_rejects_wrong_tensors_without_gpu(la):
+    import torch
+    # The binding's own checks fire before the library is reached.
+    obj = la.LinAttn.__new__(la.LinAttn)
+    obj.heads, obj.head_dim, obj.max_tokens = 2, 32, 64
+    cpu = torch.device("cpu")
+    q = torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16)
+    den = torch.ones(1, 2, 8, 1)
+    assert obj._check_inputs(q, q, q, den, cpu) == 8
+    with pytest.raises(TypeError):
+        obj._check_inputs(q.float(), q, q, den, cpu)
+    with pytest.raises(TypeError):
+        obj._check_inputs(q, q, q, den.double(), cpu)
+    with pytest.raises(ValueError):
+        obj._check_inputs(q.expand(2, 2, 8, 32), q, q, den, cpu)
+    with pytest.raises(ValueError):
+        obj._check_inputs(q, q, q, torch.ones(1, 2, 8), cpu)
+    with pytest.raises(ValueError):
+        obj._check_inputs(q.transpose(2, 3).contiguous().transpose(2, 3), q, q, den, cpu)
+    with pytest.raises(ValueError):
+        obj._check_inputs(torch.zeros(1, 3, 8, 32, dtype=torch.bfloat16), q, q, den, cpu)
+    with pytest.raises(ValueError):
+        la._mode("fast")
+    with pytest.raises(TypeError):
+        la._out_code(torch.float16)

@@ -1,0 +1,230 @@
+"""Parity of the CUDA path (through the C ABI) with the FP64 oracle on the same seeded
+inputs.  Tolerances: whole-tensor relative L2 <= 2e-5 for FP32 output and <= 4e-3 for
+BF16 output; the reduced KV <= 1e-6; repeated calls bitwise identical.  Both quality
+tiers have the same exact target, so both are held to the same bounds."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import rel_l2
+from video_diffusion_dit_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 2e-5, torch.bfloat16: 4e-3}
+KV_TOL = 1e-6
+MODES = ("high", "lossless")
+
+
+@pytest.fixture(scope="module")
+def la():
+    from video_diffusion_dit_gb300 import lin_attn
+    return lin_attn
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    return d
+
+
+def to_dev(layer, dev):
+    return {k: t.to(dev) for k, t in layer.items()}
+
+
+def run(ctx, g, mode, dt):
+    out = ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], mode=mode, out_dtype=dt)
+    assert ctx.device_status() == 0
+    return out
+
+
+def check_full(la, dev, H, N, D, seed=0, grid=None, modes=MODES, dtypes=(torch.float32, torch.bfloat16)):
+    layer = synth.make_layer(H, N, D, seed, grid)
+    qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+    kv_ref = oracle.kv(kb, vb)
+    ref = oracle.apply_rows(qb, kv_ref, den).reshape(H, N, D)
+    g = to_dev(layer, dev)
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in modes:
+            for dt in dtypes:
+                out = run(ctx, g, mode, dt)
+                err = rel_l2(out.double().cpu().numpy()[0], ref)
+                assert err <= TOL[dt], f"H={H} N={N} D={D} {mode} {dt}: rel-L2 {err:.3e}"
+                kv_err = rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref)
+                assert kv_err <= KV_TOL, f"H={H} N={N} D={D} {mode}: KV rel-L2 {kv_err:.3e}"
+
+
+def test_worked_example_bit_exact(la, dev):
+    q = torch.zeros(1, 1, 2, 16, dtype=torch.bfloat16)
+    k, v = torch.zeros_like(q), torch.zeros_like(q)
+    q[0, 0, :, :2] = torch.tensor([[1.0, 1.0], [2.0, 0.0]])
+    k[0, 0, :, :2] = torch.tensor([[1.0, 2.0], [0.0, 1.0]])
+    v[0, 0, :, :2] = torch.tensor([[1.0, 2.0], [3.0, 4.0]])
+    den = torch.tensor([2.0, 4.0]).reshape(1, 1, 2, 1)
+    want = torch.zeros(1, 1, 2, 16, dtype=torch.float64)
+    want[0, 0, :, :2] = torch.tensor([[3.0, 5.0], [0.5, 1.0]])
+    with la.LinAttn(1, 2, 16, dev) as ctx:
+        for mode in MODES:
+            for dt in (torch.float32, torch.bfloat16):
+                out = ctx.forward(q.to(dev), k.to(dev), v.to(dev), den.to(dev), mode=mode, out_dtype=dt)
+                assert torch.equal(out.double().cpu(), want), (mode, dt, out)
+                kv = ctx.debug_kv().cpu()
+                assert torch.equal(kv[0, :2, :2], torch.tensor([[1.0, 2.0], [5.0, 8.0]]))
+
+
+def test_tiny_config(la, dev):
+    check_full(la, dev, 2, 256, 32)
+
+
+@pytest.mark.parametrize("D", [16, 32, 48, 64, 80, 96, 112, 128])
+def test_head_dims(la, dev, D):
+    check_full(la, dev, 3, 777, D, seed=D)
+
+
+@pytest.mark.parametrize("N", [1, 2, 63, 64, 65, 127, 128, 129, 1000, 4097])
+def test_ragged_token_counts(la, dev, N):
+    check_full(la, dev, 2, N, 112, seed=N)
+
+
+def test_many_heads_d64(la, dev):
+    check_full(la, dev, 32, 3000, 64, seed=5)
+
+
+def test_480p_full_all_modes(la, dev):
+    w = synth.WORKLOADS["480p_81f"]
+    check_full(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid)
+
+
+def sampled_rows(H, N, count, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(H * N, size=count, replace=False)
+    edges = [0, N - 1, N, H * N - 1, (H - 1) * N, 127, 128, N - 128, N - 129]
+    return np.unique(np.concatenate([rows, [r for r in edges if 0 <= r < H * N]])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["720p_193f", "720p_193f_d64"])
+def test_full_size_sampled(la, dev, name):
+    """Full-size layer in the bench's launch configuration: KV checked whole, output on
+    sampled rows (the first/last rows of heads, tile edges and random rows)."""
+    w = synth.WORKLOADS[name]
+    H, N, D = w.heads, w.tokens, w.head_dim
+    layer = synth.make_workload(w, device=dev)
+    qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+    kv_ref = oracle.kv(kb, vb)
+    rows = sampled_rows(H, N, 4096, 1)
+    ref = oracle.apply_rows(qb, kv_ref, den, rows)
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in MODES:
+            for dt in (torch.float32, torch.bfloat16):
+                out = run(ctx, layer, mode, dt)
+                got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+                err = rel_l2(got, ref)
+                assert err <= TOL[dt], f"{name} {mode} {dt}: sampled rel-L2 {err:.3e}"
+                kv_err = rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref)
+                assert kv_err <= KV_TOL, f"{name} {mode}: KV rel-L2 {kv_err:.3e}"
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_bitwise_deterministic(la, dev, mode):
+    w = synth.WORKLOADS["480p_81f"]
+    g = synth.make_workload(w, device=dev)
+    with la.LinAttn(w.heads, w.tokens, w.head_dim, dev) as ctx:
+        a = run(ctx, g, mode, torch.float32).clone()
+        kva = ctx.debug_kv()
+        # a different call in between must leave no trace
+        run(ctx, to_dev(synth.make_layer(w.heads, 5000, w.head_dim, 3), dev), mode, torch.bfloat16)
+        b = run(ctx, g, mode, torch.float32)
+        assert torch.equal(a, b)
+        assert torch.equal(kva, ctx.debug_kv())
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_zero_v_gives_zero(la, dev, mode):
+    g = to_dev(synth.make_layer(2, 1000, 112, 4), dev)
+    g["v"].zero_()
+    with la.LinAttn(2, 1000, 112, dev) as ctx:
+        out = run(ctx, g, mode, torch.float32)
+        assert torch.count_nonzero(out).item() == 0
+
+
+def test_modes_agree_closely(la, dev):
+    g = to_dev(synth.make_layer(4, 5000, 112, 6), dev)
+    with la.LinAttn(4, 5000, 112, dev) as ctx:
+        hi = run(ctx, g, "high", torch.float32).double()
+        lo = run(ctx, g, "lossless", torch.float32).double()
+    assert (torch.linalg.norm(hi - lo) / torch.linalg.norm(lo)).item() <= 4e-5
+
+
+def test_host_buffer_path_matches_device_path(la, dev):
+    layer = synth.make_layer(3, 2000, 112, 8)
+    pinned = {k: t.pin_memory() for k, t in layer.items()}
+    g = to_dev(layer, dev)
+    with la.LinAttn(3, 4000, 112, dev) as ctx:
+        for mode in MODES:
+            for dt in (torch.float32, torch.bfloat16):
+                d = run(ctx, g, mode, dt).cpu()
+                h = ctx.forward_host(pinned["q_rot"], pinned["k_rot"], pinned["v"], pinned["den"], mode=mode,
+                                     out_dtype=dt)
+                assert torch.equal(d, h)
+        # pageable host memory works too
+        h2 = ctx.forward_host(layer["q_rot"], layer["k_rot"], layer["v"], layer["den"], out=torch.empty(
+            1, 3, 2000, 112))
+        assert torch.equal(h2, run(ctx, g, "high", torch.float32).cpu())
+
+
+def test_out_of_range_and_misaligned_calls_are_rejected(la, dev):
+    import ctypes
+    g = to_dev(synth.make_layer(2, 256, 32, 0), dev)
+    with la.LinAttn(2, 256, 32, dev) as ctx:
+        out = torch.empty(1, 2, 256, 32, device=dev)
+        h = ctx._h
+        args = [g["q_rot"].data_ptr(), g["k_rot"].data_ptr(), g["v"].data_ptr(), g["den"].data_ptr(),
+                out.data_ptr()]
+        s = torch.cuda.current_stream().cuda_stream
+        assert la.lib.lin_attn_forward(h, *args, 0, 257, 0, s) == la.ERR_INVALID_ARG
+        assert la.lib.lin_attn_forward(h, *args, 0, 0, 0, s) == la.ERR_INVALID_ARG
+        assert la.lib.lin_attn_forward(h, *args, 2, 256, 0, s) == la.ERR_INVALID_ARG
+        assert la.lib.lin_attn_forward(h, *args, 0, 256, 5, s) == la.ERR_INVALID_ARG
+        bad = list(args)
+        bad[1] += 2
+        assert la.lib.lin_attn_forward(h, *bad, 0, 256, 0, s) == la.ERR_MISALIGNED
+        with pytest.raises(ValueError):
+            ctx.forward(g["q_rot"].cpu(), g["k_rot"], g["v"], g["den"])
+        with pytest.raises(la.LinAttnError) as exc:
+            ctx.forward(*(synth.make_layer(2, 257, 32, 0)[k].to(dev) for k in ("q_rot", "k_rot", "v", "den")))
+        assert exc.value.status == la.ERR_INVALID_ARG
+        # a valid call still works afterwards
+        run(ctx, g, "high", torch.float32)
+        assert ctx.device_status() == 0
+
+
+def test_stage_events(la, dev):
+    g = to_dev(synth.make_layer(4, 20000, 112, 2), dev)
+    with la.LinAttn(4, 20000, 112, dev) as ctx:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ctx.set_stage_events(ev)
+        run(ctx, g, "high", torch.float32)
+        torch.cuda.synchronize()
+        t = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+        assert all(x >= 0 for x in t) and sum(t) > 0
+
+
+@pytest.mark.parametrize("N", [3000, 1000, 2080, 4127])
+def test_ragged_tail_stores_repeated(la, dev, N):
+    """Ragged last tiles where whole 32-row boxes lie past the end of a head: the apply
+    epilogue must not recycle a staging buffer whose store is still in flight.  The race
+    this guards against was intermittent, so the call is repeated."""
+    H, D = 24, 112 if N % 2 else 64
+    layer = synth.make_layer(H, N, D, seed=N)
+    qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+    ref = oracle.forward(qb, kb, vb, den)
+    g = to_dev(layer, dev)
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for dt in (torch.float32, torch.bfloat16):
+            first = run(ctx, g, "high", dt).clone()
+            err = rel_l2(first.double().cpu().numpy()[0], ref)
+            assert err <= TOL[dt], f"N={N} {dt}: rel-L2 {err:.3e}"
+            for _ in range(8):
+                assert torch.equal(run(ctx, g, "high", dt), first)

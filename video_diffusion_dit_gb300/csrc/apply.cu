@@ -1,0 +1,412 @@
+// Second GEMM + normalisation of SANA-Video linear attention:
+//     out[h][n][:] = (Q_rot[h][n][:] . KV[h]) / den[h][n]
+//
+// Page "PR #35728 完整报告 - [diffusion] Accelerate SANA-Video linear attention in
+// quality=high", 关键源码片段: (scores @ query_rotate.float()) * normalizer, and the
+// page's note that the second GEMM stays FP32 in both tiers.  The page multiplies by a
+// precomputed reciprocal; here each token's denominator is turned into a correctly rounded
+// reciprocal once and the row is multiplied by it (within 1 ulp of a true division).
+#include <cuda_bf16.h>
+
+#include "lin_attn_internal.cuh"
+#include "ptx.cuh"
+
+namespace la {
+namespace {
+
+// ============================================================================ tensor cores
+// Persistent: each CTA owns a contiguous range of 128-token tiles in (head, tile) order.
+// Warp 0 streams Q tiles with TMA (two 64-column boxes, 128-byte swizzle = K-major MMA
+// layout) and, when the head changes, bulk-copies that head's KV image (three BF16 terms
+// KV = hi + mid + lo, already in the swizzled K-major B layout) into shared memory.
+// Warp 1 issues, per tile, 3 terms x (Dpad / 16) MMAs of 128 x D x 16 into one of two TMEM
+// accumulators.  Warps 2..5 read the accumulator (one token row per thread), multiply by
+// the reciprocal denominator and write 32-row boxes through swizzled staging with TMA
+// stores.  BF16 x BF16 products are exact in FP32 and the three terms carry 24 bits of
+// KV, so the result has FP32-class accuracy (the tier's second GEMM "stays FP32").
+constexpr int kApplyStages = 3;
+constexpr int kApplyThreads = 192;
+constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
+constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
+
+__host__ __device__ inline uint32_t apply_smem_bytes(int head_dim) {
+    const uint32_t nbox = head_dim_atoms(head_dim);
+    return static_cast<uint32_t>(kv_image_bytes(head_dim)) + kApplyStages * nbox * kQAtomBytes +
+           4 * 2 * kOutBoxBytes + 256 + 1024;
+}
+
+template <int NBOX, bool OUT_BF16>
+__global__ void __launch_bounds__(kApplyThreads, 1)
+    apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
+                    const uint8_t* __restrict__ kv_image, const float* __restrict__ den, int heads, int n_tokens,
+                    int head_dim, int tiles_per_head, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+
+    const uint32_t img_bytes = 3u * NBOX * head_dim * 128u;
+    const uint32_t term_bytes = NBOX * head_dim * 128u;
+    const uint32_t b_smem = base;
+    const uint32_t q_smem = b_smem + img_bytes;
+    const uint32_t o_smem = q_smem + kApplyStages * NBOX * kQAtomBytes;
+    const uint32_t bar_off = img_bytes + kApplyStages * NBOX * kQAtomBytes + 8 * kOutBoxBytes;
+    const uint32_t bars = base + bar_off;
+    const uint32_t q_full0 = bars;                        // [kApplyStages]
+    const uint32_t q_empty0 = bars + 8u * kApplyStages;   // [kApplyStages]
+    const uint32_t acc_full0 = bars + 16u * kApplyStages; // [2]
+    const uint32_t acc_empty0 = acc_full0 + 16u;          // [2]
+    const uint32_t b_full = acc_empty0 + 16u;
+    const uint32_t b_empty = b_full + 8u;
+    const uint32_t drain_bar = b_empty + 8u;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + 192);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + 200);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total = heads * tiles_per_head;
+    const int t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+    const int t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kApplyStages; ++s) {
+            mbar_init(q_full0 + 8u * s, 1);
+            mbar_init(q_empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full0 + 8u * b, 1);
+            mbar_init(acc_empty0 + 8u * b, 4);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), 256);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_out);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer
+            uint32_t it = 0;
+            int cur_h = -1, run = -1;
+            bool ok = true, b_pending = false;
+            for (int t = t_begin; t < t_end; ++t, ++it) {
+                const int h = t / tiles_per_head;
+                const int n0 = (t % tiles_per_head) * kApplyTile;
+                const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
+                if (!mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kQAtomBytes);
+#pragma unroll
+                for (int x = 0; x < NBOX; ++x)
+                    tma_load_3d(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x, n0, h);
+                if (h != cur_h) {
+                    ++run;
+                    cur_h = h;
+                    if (run > 0 && !mbar_wait(b_empty, (run - 1) & 1, abort_flag, status)) {
+                        ++it;
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(b_full, img_bytes);
+                    bulk_load(b_smem, kv_image + static_cast<int64_t>(h) * img_bytes, img_bytes, b_full);
+                    b_pending = true;
+                }
+            }
+            if (!ok) {
+                const uint32_t first = it > kApplyStages ? it - kApplyStages : 0;
+                for (uint32_t j = first; j < it; ++j)
+                    mbar_wait_drain(q_full0 + 8u * (j % kApplyStages), (j / kApplyStages) & 1u);
+                if (b_pending) mbar_wait_drain(b_full, run & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idesc = make_idesc_bf16_f32(128, head_dim, false, false);
+            uint32_t it = 0;
+            int cur_h = -1, run = -1;
+            for (int t = t_begin; t < t_end; ++t, ++it) {
+                const int h = t / tiles_per_head;
+                const uint32_t lt = static_cast<uint32_t>(t - t_begin);
+                if (h != cur_h) {
+                    if (run >= 0) mma_commit(b_empty);  // old image free once its MMAs are done
+                    ++run;
+                    cur_h = h;
+                    if (!mbar_wait(b_full, run & 1, abort_flag, status)) break;
+                    tc_fence_after();
+                }
+                const uint32_t buf = lt & 1u;
+                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+                tc_fence_after();
+                const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
+                if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + buf * 128u;
+                const uint32_t qa = q_smem + st * NBOX * kQAtomBytes;
+                // Smallest term first; every product is exact, the accumulator is FP32.
+#pragma unroll
+                for (int term = 2; term >= 0; --term) {
+#pragma unroll
+                    for (int ks = 0; ks < 4 * NBOX; ++ks) {
+                        const uint32_t x = ks >> 2, off = (ks & 3) * 32u;
+                        const uint64_t ad = make_smem_desc(qa + x * kQAtomBytes + off, 16u, 1024u, kSwizzle128B);
+                        const uint64_t bd = make_smem_desc(b_smem + term * term_bytes + x * head_dim * 128u + off,
+                                                           16u, 1024u, kSwizzle128B);
+                        mma_bf16(d, ad, bd, idesc, (term != 2 || ks != 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(q_empty0 + 8u * st);
+                mma_commit(acc_full0 + 8u * buf);
+            }
+            mma_commit(drain_bar);
+            mbar_wait_drain(drain_bar, 0);
+        }
+    } else {
+        // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes / tile rows 32q..32q+31
+        const int q = warp & 3;
+        const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
+        uint32_t nstore = 0;
+        constexpr int kCols = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
+        const int groups = (head_dim + kCols - 1) / kCols;
+        for (int t = t_begin; t < t_end; ++t) {
+            const int h = t / tiles_per_head;
+            const int n0 = (t % tiles_per_head) * kApplyTile;
+            const uint32_t lt = static_cast<uint32_t>(t - t_begin);
+            const int row0 = n0 + 32 * q;
+            const int row = row0 + lane;
+            const float dv = row < n_tokens ? den[static_cast<int64_t>(h) * n_tokens + row] : 1.0f;
+            const float rcp = __frcp_rn(dv);
+            const uint32_t buf = lt & 1u;
+            if (!mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
+            // A warp whose 32 rows all lie past the end of the head (ragged last tile) has
+            // nothing to store.  It must not touch its staging buffers either: every buffer
+            // write is paired with one committed store, which is what lets wait_group.read 1
+            // guarantee the buffer's previous store has finished reading it.
+            const int live_groups = row0 < n_tokens ? groups : 0;
+            for (int g = 0; g < live_groups; ++g) {
+                uint32_t packed[32];
+                if (!OUT_BF16) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(taddr + 32u * g, r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) packed[e] = __float_as_uint(__uint_as_float(r[e]) * rcp);
+                } else {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        tmem_ld32_sync(taddr + 64u * g + 32u * half, r);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(r[2 * e]) * rcp,
+                                                                           __uint_as_float(r[2 * e + 1]) * rcp);
+                            packed[16 * half + e] = *reinterpret_cast<const uint32_t*>(&p);
+                        }
+                    }
+                }
+                const uint32_t sbuf = stage0 + (nstore & 1u) * kOutBoxBytes;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t addr = sbuf + lane * 128u + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[4 * c]),
+                                 "r"(packed[4 * c + 1]), "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tm_out, sbuf, kCols * g, row0, h);
+                    bulk_commit();
+                }
+                ++nstore;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty0 + 8u * buf);
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ============================================================================ CUDA cores
+// 'lossless': Q upcast to FP32 (exact), FP32 FMA against KV held in shared memory.
+// Persistent blocks over contiguous ranges of 64-token tiles; thread (tn, tj) owns tokens
+// 4tn..4tn+3 and columns tj + 16b.  Sums run over i in ascending order.
+constexpr int kFfmaTile = 64;
+
+__host__ __device__ inline size_t apply_ffma_smem_bytes(int head_dim) {
+    return (static_cast<size_t>(head_dim) * head_dim + static_cast<size_t>(kFfmaTile) * (head_dim + 1)) *
+           sizeof(float);
+}
+
+template <int C, bool OUT_BF16>
+__global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restrict__ q, const float* __restrict__ kv,
+                                                         const float* __restrict__ den, void* __restrict__ out,
+                                                         int heads, int n_tokens, int tiles_per_head) {
+    constexpr int D = 16 * C;
+    extern __shared__ float sm[];
+    float* kvs = sm;           // [D][D]
+    float* qt = sm + D * D;    // [D][kFfmaTile] (transposed Q tile), reused as [kFfmaTile][D + 1] output
+    const int total = heads * tiles_per_head;
+    const int t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+    const int t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    const int tn = threadIdx.x & 15, tj = threadIdx.x >> 4;
+    int cur_h = -1;
+    for (int t = t_begin; t < t_end; ++t) {
+        const int h = t / tiles_per_head;
+        const int n0 = (t % tiles_per_head) * kFfmaTile;
+        const int rows = min(kFfmaTile, n_tokens - n0);
+        const int64_t row_base = static_cast<int64_t>(h) * n_tokens + n0;
+        __syncthreads();
+        if (h != cur_h) {
+            const float4* src = reinterpret_cast<const float4*>(kv + static_cast<int64_t>(h) * D * D);
+            for (int idx = threadIdx.x; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(kvs)[idx] = src[idx];
+            cur_h = h;
+        }
+        for (int idx = threadIdx.x; idx < kFfmaTile * (D / 8); idx += 256) {
+            const int r = idx % kFfmaTile, c = idx / kFfmaTile;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (r < rows) w = *reinterpret_cast<const uint4*>(q + (row_base + r) * D + 8 * c);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                qt[(8 * c + 2 * e) * kFfmaTile + r] = __uint_as_float(ww[e] << 16);
+                qt[(8 * c + 2 * e + 1) * kFfmaTile + r] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+        }
+        __syncthreads();
+        float acc[4][C];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < C; ++b) acc[a][b] = 0.f;
+        for (int i = 0; i < D; ++i) {
+            const float4 qv = *reinterpret_cast<const float4*>(qt + i * kFfmaTile + 4 * tn);
+            float kr[C];
+#pragma unroll
+            for (int b = 0; b < C; ++b) kr[b] = kvs[i * D + tj + 16 * b];
+#pragma unroll
+            for (int b = 0; b < C; ++b) {
+                acc[0][b] = fmaf(qv.x, kr[b], acc[0][b]);
+                acc[1][b] = fmaf(qv.y, kr[b], acc[1][b]);
+                acc[2][b] = fmaf(qv.z, kr[b], acc[2][b]);
+                acc[3][b] = fmaf(qv.w, kr[b], acc[3][b]);
+            }
+        }
+        __syncthreads();
+        float* ys = qt;  // [kFfmaTile][D + 1]
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int r = 4 * tn + a;
+            const float rcp = r < rows ? __frcp_rn(den[row_base + r]) : 0.f;
+#pragma unroll
+            for (int b = 0; b < C; ++b) ys[r * (D + 1) + tj + 16 * b] = acc[a][b] * rcp;
+        }
+        __syncthreads();
+        if (!OUT_BF16) {
+            float* o = reinterpret_cast<float*>(out) + row_base * D;
+            for (int idx = threadIdx.x; idx < rows * D; idx += 256) o[idx] = ys[(idx / D) * (D + 1) + idx % D];
+        } else {
+            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + row_base * D);
+            for (int idx = threadIdx.x; idx < rows * D / 2; idx += 256) {
+                const int e = 2 * idx;
+                const int r = e / D, c = e % D;
+                o[idx] = __floats2bfloat162_rn(ys[r * (D + 1) + c], ys[r * (D + 1) + c + 1]);
+            }
+        }
+    }
+}
+
+template <int NBOX, bool BF16>
+cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
+                      int heads, int n_tokens, int head_dim, int grid, int* status, cudaStream_t stream) {
+    const uint32_t smem = apply_smem_bytes(head_dim);
+    cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
+    apply_tc_kernel<NBOX, BF16><<<grid, kApplyThreads, smem, stream>>>(tm_q, tm_out, img, den, heads, n_tokens,
+                                                                        head_dim, tph, status);
+    return cudaGetLastError();
+}
+
+template <int C, bool BF16>
+cudaError_t launch_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads, int n_tokens,
+                        int grid, cudaStream_t stream) {
+    const size_t smem = apply_ffma_smem_bytes(16 * C);
+    cudaError_t e = cudaFuncSetAttribute(apply_ffma_kernel<C, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int tph = (n_tokens + kFfmaTile - 1) / kFfmaTile;
+    const int total = heads * tph;
+    if (grid > total) grid = total;
+    apply_ffma_kernel<C, BF16><<<grid, 256, smem, stream>>>(q, kv, den, out, heads, n_tokens, tph);
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t dispatch_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads, int n_tokens,
+                          int head_dim, int grid, cudaStream_t stream) {
+    switch (head_dim / 16) {
+        case 1: return launch_ffma<1, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 2: return launch_ffma<2, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 3: return launch_ffma<3, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 4: return launch_ffma<4, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 5: return launch_ffma<5, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 6: return launch_ffma<6, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 7: return launch_ffma<7, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 8: return launch_ffma<8, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
+                            const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16, int grid,
+                            int* status, cudaStream_t stream) {
+    const int n = static_cast<int>(n_tokens);
+    const int total = heads * ((n + kApplyTile - 1) / kApplyTile);
+    if (grid > total) grid = total;
+    const bool one = head_dim_atoms(head_dim) == 1;
+    if (one)
+        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream)
+                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream);
+    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream)
+                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream);
+}
+
+cudaError_t launch_apply_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads,
+                              int64_t n_tokens, int head_dim, bool out_bf16, int grid, cudaStream_t stream) {
+    const int n = static_cast<int>(n_tokens);
+    return out_bf16 ? dispatch_ffma<true>(q, kv, den, out, heads, n, head_dim, grid, stream)
+                    : dispatch_ffma<false>(q, kv, den, out, heads, n, head_dim, grid, stream);
+}
+
+}  // namespace la

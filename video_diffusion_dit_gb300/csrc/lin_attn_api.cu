@@ -1,0 +1,376 @@
+// Host side of the lin_attn C ABI: argument checks, scratch ownership, TMA descriptors
+// and the three-kernel enqueue per layer call.  See include/lin_attn.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "lin_attn.h"
+#include "lin_attn_internal.cuh"
+
+struct lin_attn_ctx {
+    int device = 0;
+    int heads = 0;
+    int64_t max_tokens = 0;
+    int head_dim = 0;
+    int n_sms = 0;
+    int splits_alloc = 0;
+    float* partial = nullptr;     // [heads][splits_alloc][D][D] FP32 per-split partial sums
+    float* kv = nullptr;          // [heads][D][D] FP32 reduced KV
+    uint8_t* kv_image = nullptr;  // [heads] x three-term BF16 image for the tensor-core apply
+    int* status = nullptr;        // device status word (LIN_ATTN_ERR_TIMEOUT if a kernel gave up)
+    // host-buffer path staging, allocated on first use
+    void* st_q = nullptr;
+    void* st_k = nullptr;
+    void* st_v = nullptr;
+    float* st_den = nullptr;
+    void* st_out = nullptr;
+    // timing hook (one-shot)
+    cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
+    int n_events = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int ok() {
+    g_last_error.clear();
+    return LIN_ATTN_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(LIN_ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Makes `device` current for the scope and restores the caller's device afterwards.
+struct DeviceScope {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceScope(int device) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != device) err = cudaSetDevice(device);
+        else if (err == cudaSuccess) prev = -1;
+    }
+    ~DeviceScope() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a contiguous [H][N][D] tensor: dim 0 = D (innermost), 1 = N, 2 = H, with a
+// (box_x, box_y, 1) box and 128-byte swizzle; out-of-range elements read as zero and are
+// skipped on stores.
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t d, int64_t n,
+             int64_t h, uint32_t box_x, uint32_t box_y) {
+    auto fn = encode_fn();
+    if (!fn) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(h)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(n * d * elem_bytes)};
+    cuuint32_t box[3] = {box_x, box_y, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return LIN_ATTN_OK;
+}
+
+int splits_bound(int heads, int64_t max_tokens) {
+    // The largest split count any n_tokens <= max_tokens can produce.
+    int s0 = (la::kSplitUnitsTarget + heads - 1) / heads;
+    if (s0 < 1) s0 = 1;
+    if (s0 > la::kMaxSplits) s0 = la::kMaxSplits;
+    const int64_t by_tiles = (max_tokens + la::kKvTile - 1) / la::kKvTile;
+    return static_cast<int>(by_tiles < s0 ? by_tiles : s0);
+}
+
+void free_all(lin_attn_ctx* c) {
+    cudaFree(c->partial);
+    cudaFree(c->kv);
+    cudaFree(c->kv_image);
+    cudaFree(c->status);
+    cudaFree(c->st_q);
+    cudaFree(c->st_k);
+    cudaFree(c->st_v);
+    cudaFree(c->st_den);
+    cudaFree(c->st_out);
+}
+
+int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* den,
+               const void* out, int out_dtype, int64_t n_tokens, int mode) {
+    if (!ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx is NULL");
+    if (!q || !k || !v || !den || !out) return fail(LIN_ATTN_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (n_tokens < 1 || n_tokens > ctx->max_tokens)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "n_tokens=%lld outside [1, %lld]", (long long)n_tokens,
+                    (long long)ctx->max_tokens);
+    if (mode != LIN_ATTN_MODE_HIGH && mode != LIN_ATTN_MODE_LOSSLESS)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "mode=%d is not LIN_ATTN_MODE_HIGH/LOSSLESS", mode);
+    if (out_dtype != LIN_ATTN_OUT_F32 && out_dtype != LIN_ATTN_OUT_BF16)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "out_dtype=%d is not LIN_ATTN_OUT_F32/BF16", out_dtype);
+    return LIN_ATTN_OK;
+}
+
+int enqueue(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
+            int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream) {
+    const int H = c->heads, D = c->head_dim;
+    const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
+    const la::SplitPlan plan = la::split_plan(H, n_tokens);
+    cudaEvent_t* ev = c->n_events == 4 ? c->events : nullptr;
+    c->n_events = 0;
+    cudaError_t e;
+
+    if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (mode == LIN_ATTN_MODE_HIGH) {
+        CUtensorMap tk, tv;
+        int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kKvTile);
+        if (rc) return rc;
+        rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kKvTile);
+        if (rc) return rc;
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, H, n_tokens, D, plan, c->n_sms, c->status, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
+    } else {
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), c->partial,
+                                       H, n_tokens, D, plan, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
+    }
+    if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    e = la::launch_kv_finalize(c->partial, c->kv, mode == LIN_ATTN_MODE_HIGH ? c->kv_image : nullptr, H, D,
+                               plan.splits, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
+    if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (mode == LIN_ATTN_MODE_HIGH) {
+        CUtensorMap tq, to;
+        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kApplyTile);
+        if (rc) return rc;
+        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 32)
+                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, H, 32, 32);
+        if (rc) return rc;
+        e = la::launch_apply_tc(tq, to, c->kv_image, den, H, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
+    } else {
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), c->kv, den, out, H, n_tokens, D, bf16_out,
+                                  2 * c->n_sms, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "apply_ffma launch");
+    }
+    if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int lin_attn_version(void) { return LIN_ATTN_VERSION; }
+
+const char* lin_attn_error_string(int status) {
+    switch (status) {
+        case LIN_ATTN_OK: return "ok";
+        case LIN_ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case LIN_ATTN_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case LIN_ATTN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+        case LIN_ATTN_ERR_CUDA: return "CUDA error";
+        case LIN_ATTN_ERR_OOM: return "out of memory";
+        case LIN_ATTN_ERR_TIMEOUT: return "kernel gave up waiting on a barrier";
+        default: return "unknown status";
+    }
+}
+
+const char* lin_attn_last_error(void) { return g_last_error.c_str(); }
+
+int lin_attn_num_splits(int heads, int64_t n_tokens, int head_dim) {
+    if (heads < 1 || n_tokens < 1 || head_dim < 1) return -1;
+    return la::split_plan(heads, n_tokens).splits;
+}
+
+int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int head_dim, int device) {
+    if (!out_ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx out-pointer is NULL");
+    *out_ctx = nullptr;
+    if (heads < 1 || heads > 4096) return fail(LIN_ATTN_ERR_INVALID_ARG, "heads=%d outside [1, 4096]", heads);
+    if (max_tokens < 1 || max_tokens > (int64_t(1) << 30))
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "max_tokens=%lld outside [1, 2^30]", (long long)max_tokens);
+    if (head_dim < 16 || head_dim > 128 || head_dim % 16 != 0)
+        return fail(LIN_ATTN_ERR_UNSUPPORTED, "head_dim=%d is not a multiple of 16 in [16, 128]", head_dim);
+    if (static_cast<int64_t>(heads) * max_tokens > (int64_t(1) << 31) - 1)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "heads * max_tokens exceeds 2^31 - 1");
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    if (device < 0 || device >= count)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "device=%d outside [0, %d)", device, count);
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (major != 10 || minor != 3)
+        return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", device,
+                    major, minor);
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+
+    auto* c = new lin_attn_ctx();
+    c->device = device;
+    c->heads = heads;
+    c->max_tokens = max_tokens;
+    c->head_dim = head_dim;
+    c->n_sms = sms;
+    c->splits_alloc = splits_bound(heads, max_tokens);
+    const size_t dd = static_cast<size_t>(head_dim) * head_dim;
+    bool good = cudaMalloc(&c->partial, sizeof(float) * dd * heads * c->splits_alloc) == cudaSuccess &&
+                cudaMalloc(&c->kv, sizeof(float) * dd * heads) == cudaSuccess &&
+                cudaMalloc(&c->kv_image, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads) == cudaSuccess &&
+                cudaMalloc(&c->status, sizeof(int)) == cudaSuccess;
+    if (!good) {
+        cudaGetLastError();
+        free_all(c);
+        delete c;
+        return fail(LIN_ATTN_ERR_OOM, "device allocation of the context scratch failed");
+    }
+    // The image's padding columns (head-dim index >= D inside the last 64-column atom) stay zero.
+    if ((e = cudaMemset(c->kv_image, 0, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads)) != cudaSuccess ||
+        (e = cudaMemset(c->status, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_all(c);
+        delete c;
+        return cuda_fail(e, "context initialisation");
+    }
+    *out_ctx = c;
+    return ok();
+}
+
+int lin_attn_destroy(lin_attn_ctx* ctx) {
+    if (!ctx) return ok();
+    DeviceScope scope(ctx->device);
+    if (scope.err == cudaSuccess) cudaDeviceSynchronize();
+    free_all(ctx);
+    delete ctx;
+    return ok();
+}
+
+int lin_attn_forward(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v, const float* normalizer,
+                     void* out, int out_dtype, int64_t n_tokens, int mode, struct CUstream_st* stream) {
+    int rc = check_call(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(normalizer) || !aligned16(out))
+        return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    return enqueue(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,
+                          const float* normalizer, void* out, int out_dtype, int64_t n_tokens, int mode,
+                          struct CUstream_st* stream) {
+    int rc = check_call(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    const size_t elems_max = static_cast<size_t>(ctx->heads) * ctx->max_tokens * ctx->head_dim;
+    if (!ctx->st_q) {
+        bool good = cudaMalloc(&ctx->st_q, 2 * elems_max) == cudaSuccess &&
+                    cudaMalloc(&ctx->st_k, 2 * elems_max) == cudaSuccess &&
+                    cudaMalloc(&ctx->st_v, 2 * elems_max) == cudaSuccess &&
+                    cudaMalloc(&ctx->st_den, 4 * static_cast<size_t>(ctx->heads) * ctx->max_tokens) == cudaSuccess &&
+                    cudaMalloc(&ctx->st_out, 4 * elems_max) == cudaSuccess;
+        if (!good) {
+            cudaGetLastError();
+            cudaFree(ctx->st_q);
+            cudaFree(ctx->st_k);
+            cudaFree(ctx->st_v);
+            cudaFree(ctx->st_den);
+            cudaFree(ctx->st_out);
+            ctx->st_q = ctx->st_k = ctx->st_v = ctx->st_out = nullptr;
+            ctx->st_den = nullptr;
+            return fail(LIN_ATTN_ERR_OOM, "device allocation of the host-path staging failed");
+        }
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t elems = static_cast<size_t>(ctx->heads) * n_tokens * ctx->head_dim;
+    const size_t out_bytes = elems * (out_dtype == LIN_ATTN_OUT_BF16 ? 2 : 4);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(ctx->st_k, k_rot, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_v, v, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_q, q_rot, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_den, normalizer, 4 * static_cast<size_t>(ctx->heads) * n_tokens,
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    rc = enqueue(ctx, ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_den, ctx->st_out, out_dtype, n_tokens, mode, s);
+    if (rc) return rc;
+    if ((e = cudaMemcpyAsync(out, ctx->st_out, out_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return ok();
+}
+
+int lin_attn_debug_kv(lin_attn_ctx* ctx, float* kv_out, struct CUstream_st* stream) {
+    if (!ctx || !kv_out) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx or kv_out is NULL");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    const size_t bytes = sizeof(float) * ctx->heads * static_cast<size_t>(ctx->head_dim) * ctx->head_dim;
+    cudaError_t e = cudaMemcpyAsync(kv_out, ctx->kv, bytes, cudaMemcpyDeviceToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "debug_kv copy");
+    return ok();
+}
+
+int lin_attn_device_status(lin_attn_ctx* ctx, struct CUstream_st* stream) {
+    if (!ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx is NULL");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int h = 0;
+    if ((e = cudaMemcpy(&h, ctx->status, sizeof h, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "status read");
+    if (h != 0) {
+        cudaMemset(ctx->status, 0, sizeof(int));
+        return fail(h, "a kernel reported status %d (%s)", h, lin_attn_error_string(h));
+    }
+    return ok();
+}
+
+int lin_attn_set_stage_events(lin_attn_ctx* ctx, struct CUevent_st* const* events, int n_events) {
+    if (!ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx is NULL");
+    if (n_events == 0) {
+        ctx->n_events = 0;
+        return ok();
+    }
+    if (n_events != 4 || !events) return fail(LIN_ATTN_ERR_INVALID_ARG, "n_events must be 4 (or 0 to disarm)");
+    for (int i = 0; i < 4; ++i) {
+        if (!events[i]) return fail(LIN_ATTN_ERR_INVALID_ARG, "event %d is NULL", i);
+        ctx->events[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+    }
+    ctx->n_events = 4;
+    return ok();
+}
+
+}  // extern "C"

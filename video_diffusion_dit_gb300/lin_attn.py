@@ -1,0 +1,197 @@
+"""Python binding of liblin_attn.so (ctypes).  Argument marshalling only: every step of
+the layer runs in the library's CUDA kernels; torch supplies device memory and streams.
+
+Importing this module loads the library and raises ImportError if it has not been built
+(``python -c "import __graft_entry__ as g; g.build()"``).  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblin_attn.so")
+
+MODE_HIGH, MODE_LOSSLESS = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(7)
+
+EXPORTS = (
+    "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_host",
+    "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_num_splits",
+    "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
+)
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (__graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    sig = {
+        "lin_attn_create": ([ctypes.POINTER(p), i32, i64, i32, i32], i32),
+        "lin_attn_destroy": ([p], i32),
+        "lin_attn_forward": ([p, p, p, p, p, p, i32, i64, i32, p], i32),
+        "lin_attn_forward_host": ([p, p, p, p, p, p, i32, i64, i32, p], i32),
+        "lin_attn_debug_kv": ([p, p, p], i32),
+        "lin_attn_device_status": ([p, p], i32),
+        "lin_attn_num_splits": ([i32, i64, i32], i32),
+        "lin_attn_set_stage_events": ([p, ctypes.POINTER(p), i32], i32),
+        "lin_attn_error_string": ([i32], ctypes.c_char_p),
+        "lin_attn_last_error": ([], ctypes.c_char_p),
+        "lin_attn_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = lib.lin_attn_last_error().decode()
+        super().__init__(f"{where}: {lib.lin_attn_error_string(status).decode()} ({status}): {detail}")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise LinAttnError(status, where)
+
+
+def error_string(status: int) -> str:
+    return lib.lin_attn_error_string(status).decode()
+
+
+def num_splits(heads: int, n_tokens: int, head_dim: int) -> int:
+    return lib.lin_attn_num_splits(heads, n_tokens, head_dim)
+
+
+def _mode(mode) -> int:
+    if mode in ("high", MODE_HIGH):
+        return MODE_HIGH
+    if mode in ("lossless", MODE_LOSSLESS):
+        return MODE_LOSSLESS
+    raise ValueError(f"mode must be 'high' or 'lossless', got {mode!r}")
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.float32:
+        return OUT_F32
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    raise TypeError(f"out dtype must be float32 or bfloat16, got {dtype}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+class LinAttn:
+    """One context: scratch for layers of ``heads`` x up to ``max_tokens`` x ``head_dim``."""
+
+    def __init__(self, heads: int, max_tokens: int, head_dim: int, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        if dev.type != "cuda":
+            raise ValueError("LinAttn needs a CUDA device")
+        self.device = torch.device("cuda", dev.index if dev.index is not None else torch.cuda.current_device())
+        self.heads, self.max_tokens, self.head_dim = heads, max_tokens, head_dim
+        h = ctypes.c_void_p()
+        _check(lib.lin_attn_create(ctypes.byref(h), heads, max_tokens, head_dim, self.device.index), "lin_attn_create")
+        self._h = h
+
+    # ------------------------------------------------------------------ checks
+    def _check_inputs(self, q, k, v, den, want_device):
+        for name, t in (("q_rot", q), ("k_rot", k), ("v", v)):
+            if t.dtype != torch.bfloat16:
+                raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if den.dtype != torch.float32:
+            raise TypeError(f"normalizer must be float32, got {den.dtype}")
+        if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+            raise ValueError("q_rot, k_rot, v must share one [1, H, N, D] shape")
+        B, H, N, D = q.shape
+        if B != 1:
+            raise ValueError(f"batch must be 1, got {B}")
+        if H != self.heads or D != self.head_dim:
+            raise ValueError(f"context is for H={self.heads}, D={self.head_dim}; got H={H}, D={D}")
+        if tuple(den.shape) != (1, H, N, 1):
+            raise ValueError(f"normalizer must be [1, {H}, {N}, 1], got {tuple(den.shape)}")
+        for name, t in (("q_rot", q), ("k_rot", k), ("v", v), ("normalizer", den)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+            if t.device != want_device:
+                raise ValueError(f"{name} is on {t.device}, expected {want_device}")
+        return N
+
+    # ------------------------------------------------------------------ calls
+    def forward(self, q_rot, k_rot, v, normalizer, out=None, mode="high", out_dtype=torch.float32, stream=None):
+        """Enqueue one layer call on device tensors; returns ``out`` ([1, H, N, D])."""
+        n = self._check_inputs(q_rot, k_rot, v, normalizer, self.device)
+        if out is None:
+            out = torch.empty(q_rot.shape, dtype=out_dtype, device=self.device)
+        elif out.shape != q_rot.shape or not out.is_contiguous() or out.device != self.device:
+            raise ValueError("out must be a contiguous [1, H, N, D] tensor on the context's device")
+        st = lib.lin_attn_forward(self._h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(),
+                                  out.data_ptr(), _out_code(out.dtype), n, _mode(mode),
+                                  _stream_handle(stream, self.device))
+        _check(st, "lin_attn_forward")
+        return out
+
+    def forward_host(self, q_rot, k_rot, v, normalizer, out=None, mode="high", out_dtype=torch.float32, stream=None):
+        """One layer call on host tensors (pinned for full copy speed); blocks until ``out`` is filled."""
+        cpu = torch.device("cpu")
+        n = self._check_inputs(q_rot, k_rot, v, normalizer, cpu)
+        if out is None:
+            out = torch.empty(q_rot.shape, dtype=out_dtype, pin_memory=True)
+        elif out.shape != q_rot.shape or not out.is_contiguous() or out.device != cpu:
+            raise ValueError("out must be a contiguous [1, H, N, D] host tensor")
+        st = lib.lin_attn_forward_host(self._h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(),
+                                       normalizer.data_ptr(), out.data_ptr(), _out_code(out.dtype), n, _mode(mode),
+                                       _stream_handle(stream, self.device))
+        _check(st, "lin_attn_forward_host")
+        return out
+
+    def debug_kv(self, stream=None):
+        """Reduced KV of the last call, FP32 [H, D, D]."""
+        kv = torch.empty(self.heads, self.head_dim, self.head_dim, dtype=torch.float32, device=self.device)
+        _check(lib.lin_attn_debug_kv(self._h, kv.data_ptr(), _stream_handle(stream, self.device)), "lin_attn_debug_kv")
+        return kv
+
+    def device_status(self, stream=None) -> int:
+        """Synchronise the stream and return (clearing) the kernels' status word."""
+        return lib.lin_attn_device_status(self._h, _stream_handle(stream, self.device))
+
+    def set_stage_events(self, events):
+        """Arm 4 timing events (torch.cuda.Event(enable_timing=True)) for the next forward."""
+        if events is None:
+            _check(lib.lin_attn_set_stage_events(self._h, None, 0), "lin_attn_set_stage_events")
+            return
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+                e.record(torch.cuda.current_stream(self.device))
+        arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+        _check(lib.lin_attn_set_stage_events(self._h, arr, len(events)), "lin_attn_set_stage_events")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib.lin_attn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
