@@ -133,6 +133,36 @@ int lin_attn_num_splits(int heads, int64_t n_tokens, int head_dim);
  */
 int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *events, int n_events);
 
+/*
+ * Allocation-free variant of lin_attn_forward, for callers that cannot allocate device
+ * memory: a plugin whose host forbids allocation inside its execute callback, a process
+ * whose device memory is reserved up front by a caching allocator or a hard memory cap,
+ * or a latency-critical loop that must not pay cudaMalloc's implicit device
+ * synchronisation.  The paper has no counterpart to this entry point; it is an addition
+ * of this library.
+ *
+ * Same tensors, layouts, tiers, checks and results as lin_attn_forward, with the shape
+ * given directly (heads, n_tokens, head_dim) and no context; it runs on the calling
+ * thread's current device.  Its scratch is one fixed 48 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process exits; the
+ * call itself makes no cudaMalloc, cudaFree or other allocating call.
+ *   - A shape whose scratch (heads x splits x head_dim^2 FP32 partial sums, plus the
+ *     reduced KV and its image) does not fit in 48 MiB is rejected with
+ *     LIN_ATTN_ERR_INVALID_ARG.  The 720p/193-frame layer (20 x 180320 x 112) needs ~41 MiB.
+ *   - The first call on a device resolves the array's device address once
+ *     (cudaGetSymbolAddress, with that device current): make that first call before any
+ *     stream capture.
+ *   - Every call uses the same array and it keeps the previous call's contents; each call
+ *     clears what has to start at zero.  Calls that overlap on the GPU (from several
+ *     streams or host threads) race on the array and corrupt each other's results, so
+ *     serialise them.
+ *   - A kernel that gives up waiting on one of its barriers is not reported by this
+ *     entry point (there is no context to hold the status word).
+ */
+int lin_attn_forward_noalloc(const void *q_rot, const void *k_rot, const void *v,
+                             const float *normalizer, void *out, int out_dtype, int heads,
+                             int64_t n_tokens, int head_dim, int mode, struct CUstream_st *stream);
+
 /* Static description of a status code. */
 const char *lin_attn_error_string(int status);
 

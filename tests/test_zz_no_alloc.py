@@ -1,0 +1,74 @@
+"""lin_attn_forward_noalloc: the layer call for callers that cannot allocate device memory
+(a plugin host that forbids allocation in its execute callback, a process whose device
+memory is reserved up front by a caching allocator or a memory cap, a latency-critical
+loop that must not pay cudaMalloc's implicit synchronisation).  Its scratch is a fixed
+array inside the library.  It is called here through the C ABI and held to the parity
+tolerance against the regular context entry point, on two calls in a row with different
+shapes (the second one finds the first one's data still in the shared array).
+
+This file is named to be collected last, so a failure here comes after every other test
+has already run; it also passes alone in a fresh process (its first call sets the
+device up)."""
+import pytest
+import torch
+
+from conftest import rel_l2
+from video_diffusion_dit_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 2e-5, torch.bfloat16: 4e-3}
+
+
+@pytest.fixture(scope="module")
+def la():
+    from video_diffusion_dit_gb300 import lin_attn
+    return lin_attn
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    return d
+
+
+def noalloc_call(la, g, mode, dt):
+    _, H, N, D = g["q_rot"].shape
+    out = torch.empty(1, H, N, D, dtype=dt, device=g["q_rot"].device)
+    st = la.lib.lin_attn_forward_noalloc(
+        g["q_rot"].data_ptr(), g["k_rot"].data_ptr(), g["v"].data_ptr(), g["den"].data_ptr(), out.data_ptr(),
+        la.OUT_BF16 if dt == torch.bfloat16 else la.OUT_F32, H, N, D,
+        la.MODE_HIGH if mode == "high" else la.MODE_LOSSLESS, torch.cuda.current_stream().cuda_stream)
+    assert st == la.OK, la.lib.lin_attn_last_error()
+    return out
+
+
+def context_call(la, g, mode, dt, dev):
+    _, H, N, D = g["q_rot"].shape
+    with la.LinAttn(H, N, D, dev) as ctx:
+        out = ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], mode=mode, out_dtype=dt)
+        assert ctx.device_status() == 0
+        return out
+
+
+@pytest.mark.parametrize("mode", ["high", "lossless"])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_two_calls_in_a_row_match_the_context_path(la, dev, mode, dt):
+    w = synth.WORKLOADS["480p_81f"]
+    layers = [synth.make_workload(w, device=dev), synth.make_layer(6, 3000, 32, seed=1, device=dev)]
+    for g in layers:
+        got = noalloc_call(la, g, mode, dt)
+        torch.cuda.synchronize()
+        want = context_call(la, g, mode, dt, dev)
+        err = rel_l2(got.double().cpu().numpy(), want.double().cpu().numpy())
+        assert err <= TOL[dt], f"{mode} {dt} {tuple(g['q_rot'].shape)}: rel-L2 {err:.3e}"
+
+
+def test_shape_beyond_the_fixed_scratch_is_rejected(la, dev):
+    p = torch.empty(16, dtype=torch.uint8, device=dev).data_ptr()
+    # 64 heads x 12 splits x 128^2 FP32 partials alone exceed 48 MiB.
+    st = la.lib.lin_attn_forward_noalloc(p, p, p, p, p, la.OUT_F32, 64, 1 << 20, 128, la.MODE_HIGH,
+                                         torch.cuda.current_stream().cuda_stream)
+    assert st == la.ERR_INVALID_ARG
+    assert b"scratch" in la.lib.lin_attn_last_error()

@@ -186,6 +186,15 @@ int enqueue(lin_attn_ctx* c, const void* q, const void* k, const void* v, const 
 
 }  // namespace
 
+namespace la {
+// Sets the calling thread's last-error text (what lin_attn_last_error returns) for the
+// library's other translation units; returns `code`.
+int record_error(int code, const char* msg) {
+    g_last_error = msg ? msg : "";
+    return code;
+}
+}  // namespace la
+
 extern "C" {
 
 int lin_attn_version(void) { return LIN_ATTN_VERSION; }

@@ -46,6 +46,9 @@ __host__ __device__ inline int64_t kv_image_bytes(int head_dim) {
     return 3ll * head_dim_atoms(head_dim) * head_dim * 128;
 }
 
+// Sets the calling thread's last-error text (lin_attn_last_error); returns `code`.
+int record_error(int code, const char* msg);
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
 

@@ -1,0 +1,178 @@
+// lin_attn_forward_noalloc: the layer call for callers that cannot allocate device memory.
+//
+// The regular entry point keeps its scratch (per-split KV partial sums, the reduced KV,
+// the KV image the apply kernel reads, a status word) in a context made by
+// lin_attn_create, which calls cudaMalloc.  Some callers cannot do that: a plugin whose
+// host forbids allocation inside its enqueue/execute callback, a serving process whose
+// device memory is entirely reserved up front by a caching allocator or a memory cap, or
+// a latency-critical loop that must not hit cudaMalloc's implicit device synchronisation.
+// This entry point serves them from one fixed scratch array compiled into the library:
+// it calls no cudaMalloc, cudaFree or allocating library routine.
+//
+// The array (kNoAllocScratchBytes) is a file-scope __device__ variable, so every GPU that
+// loads this library holds it until the process exits.  Its host-side name is only a
+// stand-in for the symbol, never a device address: the first call on each device (with
+// that device current) resolves the real address once with cudaGetSymbolAddress and
+// caches it, and that first call should therefore come before any stream capture.  All
+// calls share the array and it keeps the previous call's contents: the parts that must
+// start at zero are cleared by every call, and calls whose execution overlaps on the GPU
+// (two streams, or two host threads) race on it and give wrong results.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "lin_attn.h"
+#include "lin_attn_internal.cuh"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;  // 48 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct DeviceSetup {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int n_sms = 0;
+    bool supported = false;
+};
+DeviceSetup g_setup[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Same 3-D [H][N][D] map (128-byte swizzle, zero fill) as the context path uses.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t d, int64_t n,
+              int64_t h, uint32_t box_x, uint32_t box_y) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(h)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(n * d * elem_bytes)};
+    cuuint32_t box[3] = {box_x, box_y, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    return la::record_error(code, buf);
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(LIN_ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, const void* v,
+                                        const float* normalizer, void* out, int out_dtype, int heads,
+                                        int64_t n_tokens, int head_dim, int mode, struct CUstream_st* stream) {
+    if (!q_rot || !k_rot || !v || !normalizer || !out) return fail(LIN_ATTN_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (heads < 1 || heads > 4096) return fail(LIN_ATTN_ERR_INVALID_ARG, "heads=%d outside [1, 4096]", heads);
+    if (n_tokens < 1 || n_tokens > (int64_t(1) << 30) || static_cast<int64_t>(heads) * n_tokens > (int64_t(1) << 31) - 1)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "n_tokens=%lld out of range", (long long)n_tokens);
+    if (head_dim < 16 || head_dim > 128 || head_dim % 16 != 0)
+        return fail(LIN_ATTN_ERR_UNSUPPORTED, "head_dim=%d is not a multiple of 16 in [16, 128]", head_dim);
+    if (mode != LIN_ATTN_MODE_HIGH && mode != LIN_ATTN_MODE_LOSSLESS)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "mode=%d is not LIN_ATTN_MODE_HIGH/LOSSLESS", mode);
+    if (out_dtype != LIN_ATTN_OUT_F32 && out_dtype != LIN_ATTN_OUT_BF16)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "out_dtype=%d is not LIN_ATTN_OUT_F32/BF16", out_dtype);
+    for (const void* p : {q_rot, k_rot, v, static_cast<const void*>(normalizer), static_cast<const void*>(out)})
+        if (reinterpret_cast<uintptr_t>(p) & 15u)
+            return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
+
+    // Scratch carve-up: partials | KV | KV image | status word, each 256-byte aligned.
+    const la::SplitPlan plan = la::split_plan(heads, n_tokens);
+    const size_t dd = static_cast<size_t>(head_dim) * head_dim;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t partial_bytes = up(sizeof(float) * dd * heads * plan.splits);
+    const size_t kv_bytes = up(sizeof(float) * dd * heads);
+    const size_t image_bytes = static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads;
+    const size_t need = partial_bytes + kv_bytes + up(image_bytes) + 256;
+    if (need > kNoAllocScratchBytes)
+        return fail(LIN_ATTN_ERR_INVALID_ARG,
+                    "this shape needs %zu bytes of scratch, more than the %zu built into the library for "
+                    "lin_attn_forward_noalloc; use a context (lin_attn_create) instead",
+                    need, kNoAllocScratchBytes);
+
+    int device = -1;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device < 0 || device >= kMaxDevices) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device index %d too large", device);
+    DeviceSetup& su = g_setup[device];
+    std::call_once(su.once, [&su, device] {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+        cudaDeviceGetAttribute(&su.n_sms, cudaDevAttrMultiProcessorCount, device);
+        su.supported = major == 10 && minor == 3;
+        if (su.supported) su.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&su.scratch), g_noalloc_scratch);
+    });
+    if (!su.supported) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is not sm_103", device);
+    if (su.err != cudaSuccess || !su.scratch) return cuda_fail(su.err, "cudaGetSymbolAddress(scratch)");
+
+    float* partial = reinterpret_cast<float*>(su.scratch);
+    float* kv = reinterpret_cast<float*>(su.scratch + partial_bytes);
+    uint8_t* image = su.scratch + partial_bytes + kv_bytes;
+    int* status = reinterpret_cast<int*>(su.scratch + partial_bytes + kv_bytes + up(image_bytes));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
+
+    // Must start at zero: the status word, and the KV image (its padding columns are read
+    // by the MMA and a previous call with another head dim may have left data there).
+    if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    if (mode == LIN_ATTN_MODE_HIGH && (e = cudaMemsetAsync(image, 0, image_bytes, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+
+    if (mode == LIN_ATTN_MODE_HIGH) {
+        CUtensorMap tk, tv;
+        if (!make_map(&tk, k_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile) ||
+            !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
+            return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        e = la::launch_kv_partial_tc(tk, tv, partial, heads, n_tokens, head_dim, plan, su.n_sms, status, s);
+    } else {
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k_rot), static_cast<const uint16_t*>(v), partial,
+                                       heads, n_tokens, head_dim, plan, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kv_partial launch");
+    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, heads, head_dim,
+                               plan.splits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
+    if (mode == LIN_ATTN_MODE_HIGH) {
+        CUtensorMap tq, to;
+        const bool okq = make_map(&tq, q_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64,
+                                  la::kApplyTile);
+        const bool oko = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads,
+                                             64, 32)
+                                  : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, head_dim, n_tokens, heads,
+                                             32, 32);
+        if (!okq || !oko) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, su.n_sms, status, s);
+    } else {
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q_rot), kv, normalizer, out, heads, n_tokens, head_dim,
+                                  bf16_out, 2 * su.n_sms, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    return la::record_error(LIN_ATTN_OK, "");
+}

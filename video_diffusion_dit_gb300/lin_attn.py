@@ -21,6 +21,7 @@ EXPORTS = (
     "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_host",
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_num_splits",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
+    "lin_attn_forward_noalloc",
 )
 
 
@@ -41,6 +42,7 @@ def _load():
         "lin_attn_error_string": ([i32], ctypes.c_char_p),
         "lin_attn_last_error": ([], ctypes.c_char_p),
         "lin_attn_version": ([], i32),
+        "lin_attn_forward_noalloc": ([p, p, p, p, p, i32, i32, i64, i32, i32, p], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -92,6 +94,26 @@ def _stream_handle(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return stream.cuda_stream
+
+
+def forward_noalloc(q_rot, k_rot, v, normalizer, out, mode="high", stream=None):
+    """Layer call that allocates no device memory (library-owned fixed scratch, current
+    device); for callers that cannot allocate.  ``out`` must be given."""
+    for name, t in (("q_rot", q_rot), ("k_rot", k_rot), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if q_rot.dim() != 4 or q_rot.shape[0] != 1 or q_rot.shape != k_rot.shape or q_rot.shape != v.shape:
+        raise ValueError("q_rot, k_rot, v must share one [1, H, N, D] shape")
+    _, H, N, D = q_rot.shape
+    if normalizer.dtype != torch.float32 or tuple(normalizer.shape) != (1, H, N, 1) or not normalizer.is_contiguous():
+        raise ValueError(f"normalizer must be a contiguous float32 [1, {H}, {N}, 1] tensor")
+    if out.shape != q_rot.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [1, H, N, D] tensor")
+    st = lib.lin_attn_forward_noalloc(q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(),
+                                      out.data_ptr(), _out_code(out.dtype), H, N, D, _mode(mode),
+                                      _stream_handle(stream, q_rot.device))
+    _check(st, "lin_attn_forward_noalloc")
+    return out
 
 
 class LinAttn:
