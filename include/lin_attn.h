@@ -96,9 +96,12 @@ int lin_attn_forward(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, co
  * Same layer call on HOST buffers (same shapes and dtypes, any alignment).  Copies the
  * inputs to device staging owned by the context, runs the layer, copies the result
  * back and synchronises `stream` before returning: when it returns OK, `out` holds the
- * result.  The staging is allocated on the first call (LIN_ATTN_ERR_OOM if that fails)
- * and kept until lin_attn_destroy.  Page-locked host buffers give full copy bandwidth;
- * pageable ones work but copy slower.
+ * result (bitwise the same as lin_attn_forward gives).  The work is pipelined over chunks
+ * of heads: host-to-device copies, kernels (on `stream`) and device-to-host copies of
+ * different chunks overlap, on two extra streams owned by the context.  The staging,
+ * streams and events are created on the first call (LIN_ATTN_ERR_OOM if the staging
+ * cannot be allocated) and kept until lin_attn_destroy.  Page-locked host buffers give
+ * full copy bandwidth and overlap; pageable ones work but copy slower.
  */
 int lin_attn_forward_host(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
                           const float *normalizer, void *out, int out_dtype, int64_t n_tokens,

@@ -174,6 +174,21 @@ def test_host_buffer_path_matches_device_path(la, dev):
         assert torch.equal(h2, run(ctx, g, "high", torch.float32).cpu())
 
 
+def test_host_pipeline_uneven_chunks_bitwise(la, dev):
+    """20 heads run as chunks of 3 (the last one holds 2): the pipelined host path must give
+    bitwise what the device path gives, in both tiers."""
+    layer = synth.make_layer(20, 3001, 112, 12)
+    pinned = {k: t.pin_memory() for k, t in layer.items()}
+    g = to_dev(layer, dev)
+    with la.LinAttn(20, 3001, 112, dev) as ctx:
+        for mode in MODES:
+            d = run(ctx, g, mode, torch.float32).cpu()
+            for _ in range(2):
+                h = ctx.forward_host(pinned["q_rot"], pinned["k_rot"], pinned["v"], pinned["den"], mode=mode)
+                assert torch.equal(d, h)
+            assert ctx.device_status() == 0
+
+
 def test_out_of_range_and_misaligned_calls_are_rejected(la, dev):
     import ctypes
     g = to_dev(synth.make_layer(2, 256, 32, 0), dev)

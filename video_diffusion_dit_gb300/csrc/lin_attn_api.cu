@@ -28,6 +28,10 @@ struct lin_attn_ctx {
     void* st_v = nullptr;
     float* st_den = nullptr;
     void* st_out = nullptr;
+    // host-buffer pipeline: copy streams and ordering events, created on first use
+    cudaStream_t s_in = nullptr;
+    cudaStream_t s_out = nullptr;
+    cudaEvent_t ev_ready = nullptr, ev_in = nullptr, ev_comp = nullptr, ev_done = nullptr;
     // timing hook (one-shot)
     cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
     int n_events = 0;
@@ -122,6 +126,10 @@ void free_all(lin_attn_ctx* c) {
     cudaFree(c->st_v);
     cudaFree(c->st_den);
     cudaFree(c->st_out);
+    if (c->s_in) cudaStreamDestroy(c->s_in);
+    if (c->s_out) cudaStreamDestroy(c->s_out);
+    for (cudaEvent_t ev : {c->ev_ready, c->ev_in, c->ev_comp, c->ev_done})
+        if (ev) cudaEventDestroy(ev);
 }
 
 int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* den,
@@ -138,51 +146,67 @@ int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void
     return LIN_ATTN_OK;
 }
 
-int enqueue(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
-            int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream) {
+// Enqueue the three kernels for heads [h0, h0 + hc) of a layer whose tensors start at the
+// given base pointers.  The split plan is always the one of the full head count, so a
+// head range gives bitwise the same numbers as the whole layer.  `ev` (4 events or null)
+// brackets the stages.
+int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
+                  int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream, int h0, int hc,
+                  cudaEvent_t* ev) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
     const la::SplitPlan plan = la::split_plan(H, n_tokens);
-    cudaEvent_t* ev = c->n_events == 4 ? c->events : nullptr;
-    c->n_events = 0;
+    const size_t head_elems = static_cast<size_t>(n_tokens) * D;
+    const size_t dd = static_cast<size_t>(D) * D;
+    q = static_cast<const uint16_t*>(q) + h0 * head_elems;
+    k = static_cast<const uint16_t*>(k) + h0 * head_elems;
+    v = static_cast<const uint16_t*>(v) + h0 * head_elems;
+    den += h0 * static_cast<size_t>(n_tokens);
+    out = static_cast<uint8_t*>(out) + h0 * head_elems * (bf16_out ? 2 : 4);
+    float* partial = c->partial + h0 * static_cast<size_t>(plan.splits) * dd;
+    float* kv = c->kv + h0 * dd;
+    uint8_t* image = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
     cudaError_t e;
 
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (mode == LIN_ATTN_MODE_HIGH) {
         CUtensorMap tk, tv;
-        int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kKvTile);
+        int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile);
         if (rc) return rc;
-        rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kKvTile);
+        rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile);
         if (rc) return rc;
-        e = la::launch_kv_partial_tc(tk, tv, c->partial, H, n_tokens, D, plan, c->n_sms, c->status, stream);
+        e = la::launch_kv_partial_tc(tk, tv, partial, hc, n_tokens, D, plan, c->n_sms, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
     } else {
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), c->partial,
-                                       H, n_tokens, D, plan, stream);
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), partial,
+                                       hc, n_tokens, D, plan, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    e = la::launch_kv_finalize(c->partial, c->kv, mode == LIN_ATTN_MODE_HIGH ? c->kv_image : nullptr, H, D,
-                               plan.splits, stream);
+    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, hc, D, plan.splits,
+                               stream);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (mode == LIN_ATTN_MODE_HIGH) {
         CUtensorMap tq, to;
-        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, la::kApplyTile);
+        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile);
         if (rc) return rc;
-        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 32)
-                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, H, 32, 32);
+        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32)
+                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32);
         if (rc) return rc;
-        e = la::launch_apply_tc(tq, to, c->kv_image, den, H, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
+        e = la::launch_apply_tc(tq, to, image, den, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     } else {
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), c->kv, den, out, H, n_tokens, D, bf16_out,
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), kv, den, out, hc, n_tokens, D, bf16_out,
                                   2 * c->n_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     return ok();
 }
+
+// Heads per chunk of the host-buffer pipeline: about eight chunks per layer.
+int host_chunk_heads(int heads) { return heads >= 8 ? (heads + 7) / 8 : 1; }
 
 }  // namespace
 
@@ -291,8 +315,10 @@ int lin_attn_forward(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, co
         return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
     DeviceScope scope(ctx->device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
-    return enqueue(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
-                   reinterpret_cast<cudaStream_t>(stream));
+    cudaEvent_t* ev = ctx->n_events == 4 ? ctx->events : nullptr;
+    ctx->n_events = 0;
+    return enqueue_heads(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
+                         reinterpret_cast<cudaStream_t>(stream), 0, ctx->heads, ev);
 }
 
 int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,
@@ -321,20 +347,58 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
             return fail(LIN_ATTN_ERR_OOM, "device allocation of the host-path staging failed");
         }
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t elems = static_cast<size_t>(ctx->heads) * n_tokens * ctx->head_dim;
-    const size_t out_bytes = elems * (out_dtype == LIN_ATTN_OUT_BF16 ? 2 : 4);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(ctx->st_k, k_rot, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(ctx->st_v, v, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(ctx->st_q, q_rot, 2 * elems, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(ctx->st_den, normalizer, 4 * static_cast<size_t>(ctx->heads) * n_tokens,
-                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_fail(e, "host-to-device copy");
-    rc = enqueue(ctx, ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_den, ctx->st_out, out_dtype, n_tokens, mode, s);
-    if (rc) return rc;
-    if ((e = cudaMemcpyAsync(out, ctx->st_out, out_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return cuda_fail(e, "device-to-host copy");
+    if (!ctx->s_in) {
+        if ((e = cudaStreamCreateWithFlags(&ctx->s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&ctx->s_out, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamCreate");
+        for (cudaEvent_t* ev : {&ctx->ev_ready, &ctx->ev_in, &ctx->ev_comp, &ctx->ev_done})
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "cudaEventCreate");
+    }
+    // Pipeline over chunks of heads: host-to-device copies on one stream, the kernels on
+    // the caller's stream, device-to-host copies on a third, so both copy directions and
+    // the compute overlap.  Each chunk waits only for its own inputs.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int H = ctx->heads, chunk = host_chunk_heads(H);
+    const size_t head_elems = static_cast<size_t>(n_tokens) * ctx->head_dim;
+    const size_t out_es = out_dtype == LIN_ATTN_OUT_BF16 ? 2 : 4;
+    auto hptr = [](const void* p, size_t off) { return static_cast<const uint8_t*>(p) + off; };
+    auto dptr = [](void* p, size_t off) { return static_cast<uint8_t*>(p) + off; };
+    if ((e = cudaEventRecord(ctx->ev_ready, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->s_in, ctx->ev_ready, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_ready, 0)) != cudaSuccess)
+        return cuda_fail(e, "stream ordering");
+    for (int h0 = 0; h0 < H; h0 += chunk) {
+        const int hc = h0 + chunk <= H ? chunk : H - h0;
+        const size_t off = h0 * head_elems * 2, bytes = hc * head_elems * 2;
+        const size_t doff = h0 * static_cast<size_t>(n_tokens) * 4, dbytes = hc * static_cast<size_t>(n_tokens) * 4;
+        if ((e = cudaMemcpyAsync(dptr(ctx->st_k, off), hptr(k_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(dptr(ctx->st_v, off), hptr(v, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(dptr(ctx->st_q, off), hptr(q_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                cudaSuccess ||
+            (e = cudaMemcpyAsync(dptr(ctx->st_den, doff), hptr(normalizer, doff), dbytes, cudaMemcpyHostToDevice,
+                                 ctx->s_in)) != cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+        if ((e = cudaEventRecord(ctx->ev_in, ctx->s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, ctx->ev_in, 0)) != cudaSuccess)
+            return cuda_fail(e, "stream ordering");
+        rc = enqueue_heads(ctx, ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_den, ctx->st_out, out_dtype, n_tokens, mode,
+                           s, h0, hc, nullptr);
+        if (rc) return rc;
+        if ((e = cudaEventRecord(ctx->ev_comp, s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_comp, 0)) != cudaSuccess)
+            return cuda_fail(e, "stream ordering");
+        const size_t ooff = h0 * head_elems * out_es, obytes = hc * head_elems * out_es;
+        if ((e = cudaMemcpyAsync(dptr(out, ooff), dptr(ctx->st_out, ooff), obytes, cudaMemcpyDeviceToHost,
+                                 ctx->s_out)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+    }
+    if ((e = cudaEventRecord(ctx->ev_done, ctx->s_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, ctx->ev_done, 0)) != cudaSuccess)
+        return cuda_fail(e, "stream ordering");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return ok();
 }
