@@ -34,7 +34,8 @@
  *     was enqueued (except LIN_ATTN_ERR_CUDA after a failed launch) and
  *     lin_attn_last_error() gives a one-line reason for the calling thread.
  *   - Results are deterministic: for the same inputs the output is bitwise the same from
- *     run to run (the cross-CTA reduction has a fixed order that depends only on N, H, D).
+ *     run to run (the cross-CTA reduction has a fixed order that depends only on the
+ *     shape and the tier; see lin_attn_kv_plan).
  */
 #ifndef LIN_ATTN_H
 #define LIN_ATTN_H
@@ -66,7 +67,7 @@ enum lin_attn_status {
 /*
  * Create a context for layers of `heads` heads, up to `max_tokens` tokens and head dim
  * `head_dim` on CUDA device `device`.  Allocates all scratch the forward pass needs
- * (per-split partial KV sums, the reduced KV, its three-term BF16 image, a status word),
+ * (per-chunk partial KV sums, the reduced KV, its three-term BF16 image, a status word),
  * so lin_attn_forward never allocates.  head_dim must be a multiple of 16 in [16, 128];
  * smaller head dims are served by zero-padding D (padding leaves out[..., :D] unchanged).
  * 1 <= heads <= 4096, 1 <= max_tokens <= 2^30.  On success *ctx is set; on failure *ctx
@@ -85,7 +86,7 @@ int lin_attn_destroy(lin_attn_ctx *ctx);
  *                     BF16 output is rounded to nearest-even from the FP32 result
  *   n_tokens        : 1 <= n_tokens <= max_tokens of the context
  *   mode            : LIN_ATTN_MODE_HIGH or LIN_ATTN_MODE_LOSSLESS
- * Enqueues three kernels (per-split KV partial sums, fixed-order reduction, apply +
+ * Enqueues three kernels (per-chunk KV partial sums, fixed-order reduction, apply +
  * normalise) on `stream`.
  */
 int lin_attn_forward(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
@@ -122,11 +123,15 @@ int lin_attn_debug_kv(lin_attn_ctx *ctx, float *kv_out, struct CUstream_st *stre
 int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
 
 /*
- * Number of token splits per head used by the KV reduction for this shape (>= 1).  It
- * depends on (heads, n_tokens, head_dim) only - never on the GPU - which is what makes
- * the reduction order, and so the result, reproducible.  Returns -1 on bad arguments.
+ * Work split of the KV reduction for this shape and tier.  The layer's (head, 64-token
+ * tile) sequence, heads outermost, is cut into `*chunks` equal contiguous chunks (one CTA
+ * each); every chunk leaves one partial D x D sum per head it touches, and each head's
+ * partials (at most `*max_segments` for the busiest head) are added in a fixed pairwise
+ * order.  The split depends on (heads, n_tokens, mode) only - never on the GPU - which is
+ * what makes the summation order, and so the result, reproducible.  Either out-pointer
+ * may be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad arguments.
  */
-int lin_attn_num_splits(int heads, int64_t n_tokens, int head_dim);
+int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *max_segments);
 
 /*
  * Timing hook.  Arms `n_events` (must be 4) CUDA events (created with timing enabled)
@@ -149,9 +154,10 @@ int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *event
  * thread's current device.  Its scratch is one fixed 48 MiB array compiled into the
  * library, which every GPU that loads the library holds until the process exits; the
  * call itself makes no cudaMalloc, cudaFree or other allocating call.
- *   - A shape whose scratch (heads x splits x head_dim^2 FP32 partial sums, plus the
- *     reduced KV and its image) does not fit in 48 MiB is rejected with
- *     LIN_ATTN_ERR_INVALID_ARG.  The 720p/193-frame layer (20 x 180320 x 112) needs ~41 MiB.
+ *   - A shape whose scratch (heads x partial slots x head_dim^2 FP32 partial sums, plus
+ *     the reduced KV and its image; see lin_attn_kv_plan) does not fit in 48 MiB is
+ *     rejected with LIN_ATTN_ERR_INVALID_ARG.  The 720p/193-frame layer (20 x 180320 x 112)
+ *     needs ~12 MiB in the 'high' tier and ~34 MiB in the 'lossless' tier.
  *   - The first call on a device resolves the array's device address once
  *     (cudaGetSymbolAddress, with that device current): make that first call before any
  *     stream capture.

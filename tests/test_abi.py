@@ -80,21 +80,24 @@ def test_calls_on_null_context_are_rejected(la):
     assert la.lib.lin_attn_destroy(None) == la.OK
 
 
-def test_split_plan_depends_on_shape_only(la):
-    # The plan fixes the reduction order: it must be a pure function of (H, N, D),
-    # cover every token exactly once, and stay within the 64-split register budget.
-    for H in (1, 2, 12, 20, 32, 64):
+def test_kv_plan_depends_on_shape_and_tier_only(la):
+    # The plan fixes the summation order: a pure function of (H, N, tier) that keeps every
+    # head within the reduction's 160-partial budget.  Chunks of the (head, 64-token tile)
+    # sequence: G = min(target, tiles, 150 H); a head meets at most ceil(G / H) + 1 chunks.
+    for H in (1, 2, 12, 20, 32, 64, 4096):
         for N in (1, 63, 64, 65, 256, 1000, 32760, 180320, 262144):
-            S = la.num_splits(H, N, 112)
-            assert 1 <= S <= 64
-            assert S == la.num_splits(H, N, 112) == la.num_splits(H, N, 64)
-            s0 = min(64, -(-760 // H))
-            chunk = -(-(-(-N // s0)) // 64) * 64
-            assert S == -(-N // chunk)
-            assert (S - 1) * chunk < N <= S * chunk
-    assert la.num_splits(20, 180320, 112) == 38
-    assert la.num_splits(20, 32760, 112) == 37
-    assert la.num_splits(0, 10, 112) == -1
+            if H * N >= 2 ** 31:
+                continue
+            for mode, target in (("high", 152), ("lossless", 608)):
+                G, segs = la.kv_plan(H, N, mode)
+                assert (G, segs) == la.kv_plan(H, N, mode)
+                T = H * -(-N // 64)
+                assert G == min(target, T, 150 * H)
+                assert 1 <= segs <= -(-G // H) + 1 <= 160
+    assert la.kv_plan(20, 180320, "high") == (152, 9)
+    assert la.kv_plan(20, 180320, "lossless") == (608, 32)
+    with pytest.raises(la.LinAttnError):
+        la.kv_plan(0, 10, "high")
 
 
 def test_binding_rejects_wrong_tensors_without_gpu(la):

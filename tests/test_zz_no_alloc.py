@@ -67,8 +67,9 @@ def test_two_calls_in_a_row_match_the_context_path(la, dev, mode, dt):
 
 def test_shape_beyond_the_fixed_scratch_is_rejected(la, dev):
     p = torch.empty(16, dtype=torch.uint8, device=dev).data_ptr()
-    # 64 heads x 12 splits x 128^2 FP32 partials alone exceed 48 MiB.
-    st = la.lib.lin_attn_forward_noalloc(p, p, p, p, p, la.OUT_F32, 64, 1 << 20, 128, la.MODE_HIGH,
+    # 1024 heads x 2 partial slots x 128^2 FP32 partials alone exceed 48 MiB (nothing is read:
+    # the call is refused before any launch).
+    st = la.lib.lin_attn_forward_noalloc(p, p, p, p, p, la.OUT_F32, 1024, 4096, 128, la.MODE_HIGH,
                                          torch.cuda.current_stream().cuda_stream)
     assert st == la.ERR_INVALID_ARG
     assert b"scratch" in la.lib.lin_attn_last_error()

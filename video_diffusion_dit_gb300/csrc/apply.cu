@@ -95,10 +95,16 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // The next layer call's first kernel waits for this grid to complete before it touches
+    // anything, so it may be scheduled right away.
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer
+            // Q tiles are inputs of the call and may be fetched before the reduction that
+            // produces the KV image has finished; the image is loaded only after the wait.
+            bool waited = false;
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             bool ok = true, b_pending = false;
@@ -115,6 +121,10 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 for (int x = 0; x < NBOX; ++x)
                     tma_load_3d(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x, n0, h);
                 if (h != cur_h) {
+                    if (!waited) {
+                        grid_dependency_wait();
+                        waited = true;
+                    }
                     ++run;
                     cur_h = h;
                     if (run > 0 && !mbar_wait(b_empty, (run - 1) & 1, abort_flag, status)) {
@@ -351,9 +361,8 @@ cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const 
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
-    apply_tc_kernel<NBOX, BF16><<<grid, kApplyThreads, smem, stream>>>(tm_q, tm_out, img, den, heads, n_tokens,
-                                                                        head_dim, tph, status);
-    return cudaGetLastError();
+    return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
+                             img, den, heads, n_tokens, head_dim, tph, status);
 }
 
 template <int C, bool BF16>

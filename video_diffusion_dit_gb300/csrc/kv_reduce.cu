@@ -3,9 +3,12 @@
 // Page "PR #35728 完整报告 - [diffusion] Accelerate SANA-Video linear attention in
 // quality=high", 关键源码片段: the site runs the first GEMM as a BF16 bmm with FP32
 // accumulation/output ('high'); the model's fallback chain upcasts both operands to FP32
-// first ('lossless').  The token axis is cut into S splits per head (S fixed by the shape);
-// each split's D x D partial sum goes to scratch, and kv_finalize adds the S partials in a
-// fixed pairwise order, so the result is the same on every run.
+// first ('lossless').
+//
+// Work split (KvPlan): the layer's (head, 64-token tile) sequence is cut into G equal
+// contiguous chunks, one CTA each.  A chunk leaves one D x D partial sum per head it
+// touches (a "segment"); kv_finalize adds each head's partials in a fixed pairwise order.
+// G is a constant, so the order - and the result - depends on the shape alone.
 #include <cuda_bf16.h>
 
 #include "lin_attn_internal.cuh"
@@ -16,10 +19,10 @@ namespace {
 
 // ============================================================================ tensor cores
 // Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma, warps 2..5 drain the
-// TMEM accumulator to scratch.  Per stage, one 64-token tile of K and of V is loaded with
-// 128-byte swizzle as [token][64 head-dim columns] boxes - exactly the MN-major canonical
-// layout of the MMA operands A = K^T (M = head-dim row i) and B = V (N = head-dim column j),
-// with K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
+// TMEM accumulator.  Per stage, one 64-token tile of K and of V is loaded with 128-byte
+// swizzle as [token][64 head-dim columns] boxes - exactly the MN-major canonical layout of
+// the MMA operands A = K^T (M = head-dim row i) and B = V (N = head-dim column j), with
+// K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
 constexpr int kKvPromoteTiles = 4;  // tiles per tensor-core sub-chunk (256 tokens)
@@ -34,11 +37,23 @@ struct KvLayout {
     static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;  // + barriers + alignment slack
 };
 
+// Tiles [t_s, t_e) of the CTA's chunk, clipped to the launch's head range.
+struct ChunkTiles {
+    int64_t c, t_s, t_e;
+};
+__device__ __forceinline__ ChunkTiles chunk_tiles(const KvPlan& plan, const KvLaunch& work) {
+    ChunkTiles r;
+    r.c = work.c_lo + blockIdx.x;
+    r.t_s = max(chunk_begin(plan, r.c), work.t_lo);
+    r.t_e = min(chunk_begin(plan, r.c + 1), work.t_hi);
+    return r;
+}
+
 template <int NBOX>
 __global__ void __launch_bounds__(kKvThreads, 1)
     kv_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                         float* __restrict__ partial, int heads, int n_tokens, int head_dim, int chunk,
-                         int splits, int* status) {
+                         float* __restrict__ partial, int head_dim, const KvPlan plan, const KvLaunch work,
+                         int* status) {
     using L = KvLayout<NBOX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -56,7 +71,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int units = heads * splits;
+    const ChunkTiles ct = chunk_tiles(plan, work);
+    const int64_t tph = plan.tiles_per_head;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKvStages; ++s) {
@@ -92,31 +108,31 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // The prologue above overlaps the previous kernel's tail; K/V, and the partial buffer
+    // the previous layer call's reduction reads, are touched only after this.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- producer
+            // ---------------- producer: every tile of the chunk, in order
             uint32_t it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-                const int h = u / splits, s = u % splits;
-                const int t0 = s * chunk;
-                const int t1 = min(t0 + chunk, n_tokens);
-                const int ntiles = (t1 - t0 + kKvTile - 1) / kKvTile;
-                for (int k = 0; k < ntiles; ++k, ++it) {
-                    const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
-                    if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t a = base + st * L::stage_bytes;
-                    const uint32_t b = a + L::a_bytes;
-                    mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
+            for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
+                const int h = static_cast<int>(t / tph);
+                const int y = static_cast<int>((t % tph) * kKvTile);
+                const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
+                if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a = base + st * L::stage_bytes;
+                const uint32_t b = a + L::a_bytes;
+                mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
 #pragma unroll
-                    for (int x = 0; x < NBOX; ++x) {
-                        tma_load_3d(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, t0 + k * kKvTile, h);
-                        tma_load_3d(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, t0 + k * kKvTile, h);
-                    }
+                for (int x = 0; x < NBOX; ++x) {
+                    tma_load_3d(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, y, h - work.h0);
+                    tma_load_3d(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, y, h - work.h0);
                 }
             }
             if (!ok) {
@@ -129,20 +145,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
-            // Each split is accumulated in sub-chunks of kKvPromoteTiles tiles, alternating
-            // between two TMEM accumulators; the epilogue adds every finished sub-chunk into
-            // FP32 registers (round-to-nearest), so tensor-core accumulation never runs over
-            // more than kKvPromoteTiles * 64 tokens.
+            // Each segment (the chunk's tiles of one head) is accumulated in sub-chunks of
+            // kKvPromoteTiles tiles, alternating between two TMEM accumulators; the epilogue
+            // adds every finished sub-chunk into FP32 registers (round-to-nearest), so
+            // tensor-core accumulation never runs over more than 256 tokens.
             constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64 * NBOX, true, true);
             uint32_t it = 0, sub = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-                const int s = u % splits;
-                const int t0 = s * chunk;
-                const int t1 = min(t0 + chunk, n_tokens);
-                const int ntiles = (t1 - t0 + kKvTile - 1) / kKvTile;
-                for (int k0 = 0; ok && k0 < ntiles; k0 += kKvPromoteTiles, ++sub) {
-                    const int k1 = min(k0 + kKvPromoteTiles, ntiles);
+            for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
+                const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+                for (int64_t k0 = t; ok && k0 < seg_end; k0 += kKvPromoteTiles, ++sub) {
+                    const int64_t k1 = min(k0 + kKvPromoteTiles, seg_end);
                     const uint32_t buf = sub & 1u;
                     if (!mbar_wait(acc_empty0 + 8u * buf, ((sub >> 1) & 1u) ^ 1u, abort_flag, status)) {
                         ok = false;
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d = tmem + buf * 128u;
-                    for (int k = k0; k < k1; ++k, ++it) {
+                    for (int64_t k = k0; k < k1; ++k, ++it) {
                         const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
                         if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status)) {
                             ok = false;
@@ -170,26 +183,25 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     }
                     if (ok) mma_commit(acc_full0 + 8u * buf);
                 }
+                t = seg_end;
             }
             mma_commit(drain_bar);
             mbar_wait_drain(drain_bar, 0);
         }
     } else {
         // ---------------- epilogue: TMEM lanes 32q..32q+31 = rows i of the partial KV.
-        // Thread i keeps its row of the split's running sum in registers.
+        // Thread i keeps its row of the segment's running sum in registers.
         const int q = warp & 3;
         const int i = 32 * q + lane;
         uint32_t sub = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-            const int h = u / splits, s = u % splits;
-            const int t0 = s * chunk;
-            const int t1 = min(t0 + chunk, n_tokens);
-            const int ntiles = (t1 - t0 + kKvTile - 1) / kKvTile;
+        for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
+            const int h = static_cast<int>(t / tph);
+            const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
             float acc[64 * NBOX];
 #pragma unroll
             for (int c = 0; c < 64 * NBOX; ++c) acc[c] = 0.f;
-            for (int k0 = 0; k0 < ntiles; k0 += kKvPromoteTiles, ++sub) {
+            for (int64_t k0 = t; k0 < seg_end; k0 += kKvPromoteTiles, ++sub) {
                 const uint32_t buf = sub & 1u;
                 if (!mbar_wait(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status)) {
                     ok = false;
@@ -212,7 +224,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             }
             if (!ok) break;
             if (i < head_dim) {
-                float* dst = partial + ((static_cast<int64_t>(h) * splits + s) * head_dim + i) * head_dim;
+                const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
+                float* dst = partial + (slot * head_dim + i) * head_dim;
 #pragma unroll
                 for (int c = 0; c < 4 * NBOX; ++c) {
                     if (16 * c < head_dim) {
@@ -224,6 +237,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     }
                 }
             }
+            t = seg_end;
         }
     }
 
@@ -236,172 +250,228 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ============================================================================ CUDA cores
-// 'lossless': both operands upcast from BF16 to FP32 (exact), FP32 FMA, one block per
-// (split, head); thread (ti, tj) owns KV rows ti + 16a and columns tj + 16b.
+// 'lossless': both operands upcast from BF16 to FP32 (exact), FP32 FMA.  One CTA per chunk;
+// thread (ti, tj) owns KV rows ti + 16a and columns tj + 16b of the running segment sum;
+// tokens are added in ascending order, 32 at a time through shared memory.
 constexpr int kFfmaKvRows = 32;
 
 template <int C>
 __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __restrict__ k,
                                                               const uint16_t* __restrict__ v,
                                                               float* __restrict__ partial, int n_tokens,
-                                                              int chunk, int splits) {
+                                                              const KvPlan plan, const KvLaunch work) {
     constexpr int D = 16 * C;
     __shared__ float ks[kFfmaKvRows][D];
     __shared__ float vs[kFfmaKvRows][D];
-    const int s = blockIdx.x, h = blockIdx.y;
-    const int t0 = s * chunk;
-    const int t1 = min(t0 + chunk, n_tokens);
+    const ChunkTiles ct = chunk_tiles(plan, work);
+    const int64_t tph = plan.tiles_per_head;
     const int ti = threadIdx.x & 15, tj = threadIdx.x >> 4;
-    const uint16_t* kh = k + static_cast<int64_t>(h) * n_tokens * D;
-    const uint16_t* vh = v + static_cast<int64_t>(h) * n_tokens * D;
 
-    float acc[C][C];
-#pragma unroll
-    for (int a = 0; a < C; ++a)
-#pragma unroll
-        for (int b = 0; b < C; ++b) acc[a][b] = 0.f;
+    for (int64_t t = ct.t_s; t < ct.t_e;) {
+        const int h = static_cast<int>(t / tph);
+        const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+        const int n_begin = static_cast<int>((t % tph) * kKvTile);
+        const int n_end = static_cast<int>(min(static_cast<int64_t>(n_tokens), (seg_end - h * tph) * kKvTile));
+        const uint16_t* kh = k + static_cast<int64_t>(h - work.h0) * n_tokens * D;
+        const uint16_t* vh = v + static_cast<int64_t>(h - work.h0) * n_tokens * D;
 
-    for (int n0 = t0; n0 < t1; n0 += kFfmaKvRows) {
-        const int rows = min(kFfmaKvRows, t1 - n0);
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < kFfmaKvRows * (D / 8); idx += 256) {
-            const int r = idx / (D / 8), c = idx % (D / 8);
-            uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
-            if (r < rows) {
-                kw = *reinterpret_cast<const uint4*>(kh + static_cast<int64_t>(n0 + r) * D + 8 * c);
-                vw = *reinterpret_cast<const uint4*>(vh + static_cast<int64_t>(n0 + r) * D + 8 * c);
+        float acc[C][C];
+#pragma unroll
+        for (int a = 0; a < C; ++a)
+#pragma unroll
+            for (int b = 0; b < C; ++b) acc[a][b] = 0.f;
+
+        for (int n0 = n_begin; n0 < n_end; n0 += kFfmaKvRows) {
+            const int rows = min(kFfmaKvRows, n_end - n0);
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < kFfmaKvRows * (D / 8); idx += 256) {
+                const int r = idx / (D / 8), c = idx % (D / 8);
+                uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
+                if (r < rows) {
+                    kw = *reinterpret_cast<const uint4*>(kh + static_cast<int64_t>(n0 + r) * D + 8 * c);
+                    vw = *reinterpret_cast<const uint4*>(vh + static_cast<int64_t>(n0 + r) * D + 8 * c);
+                }
+                const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
+                const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ks[r][8 * c + 2 * e] = __uint_as_float(kk[e] << 16);
+                    ks[r][8 * c + 2 * e + 1] = __uint_as_float(kk[e] & 0xFFFF0000u);
+                    vs[r][8 * c + 2 * e] = __uint_as_float(vv[e] << 16);
+                    vs[r][8 * c + 2 * e + 1] = __uint_as_float(vv[e] & 0xFFFF0000u);
+                }
             }
-            const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
-            const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
+            __syncthreads();
+            for (int r = 0; r < rows; ++r) {
+                float kr[C], vr[C];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                ks[r][8 * c + 2 * e] = __uint_as_float(kk[e] << 16);
-                ks[r][8 * c + 2 * e + 1] = __uint_as_float(kk[e] & 0xFFFF0000u);
-                vs[r][8 * c + 2 * e] = __uint_as_float(vv[e] << 16);
-                vs[r][8 * c + 2 * e + 1] = __uint_as_float(vv[e] & 0xFFFF0000u);
+                for (int a = 0; a < C; ++a) kr[a] = ks[r][ti + 16 * a];
+#pragma unroll
+                for (int b = 0; b < C; ++b) vr[b] = vs[r][tj + 16 * b];
+#pragma unroll
+                for (int a = 0; a < C; ++a)
+#pragma unroll
+                    for (int b = 0; b < C; ++b) acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
             }
         }
-        __syncthreads();
-        for (int r = 0; r < rows; ++r) {
-            float kr[C], vr[C];
+        const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
+        float* dst = partial + slot * D * D;
 #pragma unroll
-            for (int a = 0; a < C; ++a) kr[a] = ks[r][ti + 16 * a];
+        for (int a = 0; a < C; ++a)
 #pragma unroll
-            for (int b = 0; b < C; ++b) vr[b] = vs[r][tj + 16 * b];
-#pragma unroll
-            for (int a = 0; a < C; ++a)
-#pragma unroll
-                for (int b = 0; b < C; ++b) acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
-        }
+            for (int b = 0; b < C; ++b) dst[(ti + 16 * a) * D + tj + 16 * b] = acc[a][b];
+        t = seg_end;
     }
-    float* dst = partial + (static_cast<int64_t>(h) * splits + s) * D * D;
-#pragma unroll
-    for (int a = 0; a < C; ++a)
-#pragma unroll
-        for (int b = 0; b < C; ++b) dst[(ti + 16 * a) * D + tj + 16 * b] = acc[a][b];
 }
 
 // ============================================================================ reduction
-// kv[h][e] = pairwise tree over the S partials: level w adds partial s + w into s for every
-// s that is a multiple of 2w.  The shape fixes S and so the order.  Also writes the
-// three-term BF16 image of KV^T for the tensor-core apply: row j, column i of term t sits
-// in 64-column atom i / 64, in the 128-byte-swizzled K-major layout (16-byte chunk
-// (i % 64) / 8 of row j stored at chunk position ((i % 64) / 8) ^ (j % 8)).
+// kv[h][i][j] = the head's partials added in a fixed pairwise order: groups of 32 partials
+// are each reduced as a tree (level w adds partial s + w into s for every s that is a
+// multiple of 2w), then the group sums are reduced the same way.  The shape fixes the
+// number of partials and so the order.
+//
+// The three-term BF16 image of KV^T is written in the apply MMA's B layout: row j,
+// columns i = 8r .. 8r+7 form one 16-byte chunk in 64-column atom r / 8 of the
+// 128-byte-swizzled K-major layout, at chunk position (r % 8) ^ (j % 8) of row j.
+constexpr int kTreeGroup = 32;
+constexpr int kTreeGroups = (kMaxSegments + kTreeGroup - 1) / kTreeGroup;
+
+template <int N>
+__device__ __forceinline__ float pairwise_sum(float (&v)[N], int count) {
+#pragma unroll
+    for (int w = 1; w < N; w *= 2) {
+#pragma unroll
+        for (int s = 0; s + w < N; s += 2 * w)
+            if (s + w < count) v[s] = v[s] + v[s + w];
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ float reduce_segments(const float* p, int64_t stride, int nseg) {
+    float groups[kTreeGroups];
+    int ngroups = 0;
+#pragma unroll
+    for (int g = 0; g < kTreeGroups; ++g) {
+        const int g0 = g * kTreeGroup;
+        if (g0 < nseg) {
+            float vals[kTreeGroup];
+#pragma unroll
+            for (int s = 0; s < kTreeGroup; ++s) vals[s] = g0 + s < nseg ? p[(g0 + s) * stride] : 0.f;
+            groups[g] = pairwise_sum(vals, nseg - g0);
+            ngroups = g + 1;
+        } else {
+            groups[g] = 0.f;
+        }
+    }
+    return pairwise_sum(groups, ngroups);
+}
+
+// A CTA reduces an 8-row x 32-column tile of one head's KV: thread (row e, column jl)
+// adds the partials of one element (loads coalesced across the 32 columns), then the
+// tile goes through shared memory so that 32 threads each write one 16-byte chunk (8
+// consecutive rows i of column j) per term of the image.
 __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restrict__ partial,
                                                           float* __restrict__ kv, uint8_t* __restrict__ image,
-                                                          int head_dim, int splits) {
-    const int h = blockIdx.y;
+                                                          int h0, int head_dim, const KvPlan plan) {
+    grid_launch_dependents();  // the apply kernel may start its prologue and Q loads now
+    grid_dependency_wait();    // the partials of this call are complete past this point
+    __shared__ float tile[8][33];
+    const int h = h0 + blockIdx.z;
     const int dd = head_dim * head_dim;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= dd) return;
-    const float* p = partial + static_cast<int64_t>(h) * splits * dd + e;
-    float vals[kMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) vals[s] = s < splits ? p[static_cast<int64_t>(s) * dd] : 0.f;
-#pragma unroll
-    for (int w = 1; w < kMaxSplits; w *= 2) {
-#pragma unroll
-        for (int s = 0; s + w < kMaxSplits; s += 2 * w)
-            if (s + w < splits) vals[s] = vals[s] + vals[s + w];
+    const int r = blockIdx.y;                // rows 8r .. 8r+7
+    const int j0 = blockIdx.x * 32;          // columns j0 .. j0+31
+    const int e = threadIdx.x >> 5, jl = threadIdx.x & 31;
+    const int i = 8 * r + e, j = j0 + jl;
+    const int nseg = segments_of_head(plan, h);
+    float x = 0.f;
+    if (j < head_dim) {
+        const float* p = partial + static_cast<int64_t>(h) * plan.seg_stride * dd + i * head_dim + j;
+        x = reduce_segments(p, dd, nseg);
+        kv[static_cast<int64_t>(h) * dd + i * head_dim + j] = x;
     }
-    const float x = vals[0];
-    kv[static_cast<int64_t>(h) * dd + e] = x;
     if (image == nullptr) return;
-
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(hi);  // exact
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);  // exact
-    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-
-    const int i = e / head_dim, j = e % head_dim;
+    tile[e][jl] = x;
+    __syncthreads();
+    if (threadIdx.x >= 32 || j0 + threadIdx.x >= head_dim) return;
+    const int jj = j0 + threadIdx.x;
+    uint32_t hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 8; u += 2) {
+        __nv_bfloat16 h2[2], m2[2], l2[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const float v = tile[u + w][threadIdx.x];
+            h2[w] = __float2bfloat16_rn(v);
+            const float r1 = v - __bfloat162float(h2[w]);  // exact
+            m2[w] = __float2bfloat16_rn(r1);
+            const float r2 = r1 - __bfloat162float(m2[w]);  // exact
+            l2[w] = __float2bfloat16_rn(r2);
+        }
+        hi[u / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h2[0])) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(h2[1])) << 16);
+        mid[u / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(m2[0])) |
+                     (static_cast<uint32_t>(__bfloat16_as_ushort(m2[1])) << 16);
+        lo[u / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(l2[0])) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(l2[1])) << 16);
+    }
     const int atoms = head_dim_atoms(head_dim);
     const int64_t term_bytes = static_cast<int64_t>(atoms) * head_dim * 128;
-    const int a = i >> 6, c = i & 63;
-    const int64_t off = static_cast<int64_t>(a) * head_dim * 128 + j * 128 + ((((c >> 3) ^ (j & 7))) << 4) + (c & 7) * 2;
+    const int64_t off = static_cast<int64_t>(r >> 3) * head_dim * 128 + jj * 128 + (((r & 7) ^ (jj & 7)) << 4);
     uint8_t* img = image + static_cast<int64_t>(h) * 3 * term_bytes + off;
-    *reinterpret_cast<__nv_bfloat16*>(img) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(img + term_bytes) = mid;
-    *reinterpret_cast<__nv_bfloat16*>(img + 2 * term_bytes) = lo;
+    *reinterpret_cast<uint4*>(img) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(img + term_bytes) = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+    *reinterpret_cast<uint4*>(img + 2 * term_bytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 template <int NBOX>
-cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int heads, int n_tokens,
-                      int head_dim, SplitPlan plan, int grid, int* status, cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int head_dim,
+                      const KvPlan& plan, const KvLaunch& work, int* status, cudaStream_t stream) {
     using L = KvLayout<NBOX>;
     cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::smem_bytes);
     if (e != cudaSuccess) return e;
-    kv_partial_tc_kernel<NBOX><<<grid, kKvThreads, L::smem_bytes, stream>>>(
-        tm_k, tm_v, partial, heads, n_tokens, head_dim, static_cast<int>(plan.chunk), plan.splits, status);
-    return cudaGetLastError();
+    return launch_overlapped(kv_partial_tc_kernel<NBOX>, dim3(work.n_chunks), dim3(kKvThreads), L::smem_bytes, stream,
+                             tm_k, tm_v, partial, head_dim, plan, work, status);
 }
 
 template <int C>
-cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, float* partial, int heads, int n_tokens,
-                        SplitPlan plan, cudaStream_t stream) {
-    dim3 grid(plan.splits, heads);
-    kv_partial_ffma_kernel<C><<<grid, 256, 0, stream>>>(k, v, partial, n_tokens, static_cast<int>(plan.chunk),
-                                                       plan.splits);
+cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, float* partial, int n_tokens, const KvPlan& plan,
+                        const KvLaunch& work, cudaStream_t stream) {
+    kv_partial_ffma_kernel<C><<<work.n_chunks, 256, 0, stream>>>(k, v, partial, n_tokens, plan, work);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int heads,
-                                 int64_t n_tokens, int head_dim, SplitPlan plan, int grid, int* status,
+cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, int* status,
                                  cudaStream_t stream) {
-    const int units = heads * plan.splits;
-    if (grid > units) grid = units;
-    if (head_dim_atoms(head_dim) == 1)
-        return launch_tc<1>(tm_k, tm_v, partial, heads, static_cast<int>(n_tokens), head_dim, plan, grid, status,
-                            stream);
-    return launch_tc<2>(tm_k, tm_v, partial, heads, static_cast<int>(n_tokens), head_dim, plan, grid, status,
-                        stream);
+    (void)n_tokens;
+    if (head_dim_atoms(head_dim) == 1) return launch_tc<1>(tm_k, tm_v, partial, head_dim, plan, work, status, stream);
+    return launch_tc<2>(tm_k, tm_v, partial, head_dim, plan, work, status, stream);
 }
 
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int heads,
-                                   int64_t n_tokens, int head_dim, SplitPlan plan, cudaStream_t stream) {
+cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int64_t n_tokens,
+                                   int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
     switch (head_dim / 16) {
-        case 1: return launch_ffma<1>(k, v, partial, heads, n, plan, stream);
-        case 2: return launch_ffma<2>(k, v, partial, heads, n, plan, stream);
-        case 3: return launch_ffma<3>(k, v, partial, heads, n, plan, stream);
-        case 4: return launch_ffma<4>(k, v, partial, heads, n, plan, stream);
-        case 5: return launch_ffma<5>(k, v, partial, heads, n, plan, stream);
-        case 6: return launch_ffma<6>(k, v, partial, heads, n, plan, stream);
-        case 7: return launch_ffma<7>(k, v, partial, heads, n, plan, stream);
-        case 8: return launch_ffma<8>(k, v, partial, heads, n, plan, stream);
+        case 1: return launch_ffma<1>(k, v, partial, n, plan, work, stream);
+        case 2: return launch_ffma<2>(k, v, partial, n, plan, work, stream);
+        case 3: return launch_ffma<3>(k, v, partial, n, plan, work, stream);
+        case 4: return launch_ffma<4>(k, v, partial, n, plan, work, stream);
+        case 5: return launch_ffma<5>(k, v, partial, n, plan, work, stream);
+        case 6: return launch_ffma<6>(k, v, partial, n, plan, work, stream);
+        case 7: return launch_ffma<7>(k, v, partial, n, plan, work, stream);
+        case 8: return launch_ffma<8>(k, v, partial, n, plan, work, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int heads, int head_dim,
-                               int splits, cudaStream_t stream) {
-    const int dd = head_dim * head_dim;
-    dim3 grid((dd + 255) / 256, heads);
-    kv_finalize_kernel<<<grid, 256, 0, stream>>>(partial, kv, kv_image, head_dim, splits);
-    return cudaGetLastError();
+cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
+                               const KvPlan& plan, cudaStream_t stream) {
+    dim3 grid((head_dim + 31) / 32, head_dim / 8, hc);
+    return launch_overlapped(kv_finalize_kernel, grid, dim3(256), 0, stream, partial, kv, kv_image, h0, head_dim,
+                             plan);
 }
 
 }  // namespace la

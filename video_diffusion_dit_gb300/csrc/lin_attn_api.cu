@@ -17,8 +17,8 @@ struct lin_attn_ctx {
     int64_t max_tokens = 0;
     int head_dim = 0;
     int n_sms = 0;
-    int splits_alloc = 0;
-    float* partial = nullptr;     // [heads][splits_alloc][D][D] FP32 per-split partial sums
+    int seg_stride_alloc = 0;
+    float* partial = nullptr;     // [heads][seg_stride_alloc][D][D] FP32 per-chunk partial sums
     float* kv = nullptr;          // [heads][D][D] FP32 reduced KV
     uint8_t* kv_image = nullptr;  // [heads] x three-term BF16 image for the tensor-core apply
     int* status = nullptr;        // device status word (LIN_ATTN_ERR_TIMEOUT if a kernel gave up)
@@ -107,15 +107,6 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     return LIN_ATTN_OK;
 }
 
-int splits_bound(int heads, int64_t max_tokens) {
-    // The largest split count any n_tokens <= max_tokens can produce.
-    int s0 = (la::kSplitUnitsTarget + heads - 1) / heads;
-    if (s0 < 1) s0 = 1;
-    if (s0 > la::kMaxSplits) s0 = la::kMaxSplits;
-    const int64_t by_tiles = (max_tokens + la::kKvTile - 1) / la::kKvTile;
-    return static_cast<int>(by_tiles < s0 ? by_tiles : s0);
-}
-
 void free_all(lin_attn_ctx* c) {
     cudaFree(c->partial);
     cudaFree(c->kv);
@@ -155,7 +146,9 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                   cudaEvent_t* ev) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
-    const la::SplitPlan plan = la::split_plan(H, n_tokens);
+    const bool tc = mode == LIN_ATTN_MODE_HIGH;
+    const la::KvPlan plan = la::kv_plan(H, n_tokens, tc);
+    const la::KvLaunch work = la::kv_launch(plan, h0, hc);
     const size_t head_elems = static_cast<size_t>(n_tokens) * D;
     const size_t dd = static_cast<size_t>(D) * D;
     q = static_cast<const uint16_t*>(q) + h0 * head_elems;
@@ -163,9 +156,8 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
     v = static_cast<const uint16_t*>(v) + h0 * head_elems;
     den += h0 * static_cast<size_t>(n_tokens);
     out = static_cast<uint8_t*>(out) + h0 * head_elems * (bf16_out ? 2 : 4);
-    float* partial = c->partial + h0 * static_cast<size_t>(plan.splits) * dd;
-    float* kv = c->kv + h0 * dd;
-    uint8_t* image = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
+    float* kv_h0 = c->kv + h0 * dd;
+    uint8_t* image_h0 = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
     cudaError_t e;
 
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -175,16 +167,15 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         if (rc) return rc;
         rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile);
         if (rc) return rc;
-        e = la::launch_kv_partial_tc(tk, tv, partial, hc, n_tokens, D, plan, c->n_sms, c->status, stream);
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
     } else {
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), partial,
-                                       hc, n_tokens, D, plan, stream);
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), c->partial,
+                                       n_tokens, D, plan, work, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, hc, D, plan.splits,
-                               stream);
+    e = la::launch_kv_finalize(c->partial, c->kv, tc ? c->kv_image : nullptr, h0, hc, D, plan, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (mode == LIN_ATTN_MODE_HIGH) {
@@ -194,10 +185,10 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32)
                       : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32);
         if (rc) return rc;
-        e = la::launch_apply_tc(tq, to, image, den, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
+        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     } else {
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), kv, den, out, hc, n_tokens, D, bf16_out,
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), kv_h0, den, out, hc, n_tokens, D, bf16_out,
                                   2 * c->n_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_ffma launch");
     }
@@ -238,9 +229,18 @@ const char* lin_attn_error_string(int status) {
 
 const char* lin_attn_last_error(void) { return g_last_error.c_str(); }
 
-int lin_attn_num_splits(int heads, int64_t n_tokens, int head_dim) {
-    if (heads < 1 || n_tokens < 1 || head_dim < 1) return -1;
-    return la::split_plan(heads, n_tokens).splits;
+int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int* chunks, int* max_segments) {
+    if (heads < 1 || n_tokens < 1 || (mode != LIN_ATTN_MODE_HIGH && mode != LIN_ATTN_MODE_LOSSLESS))
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "bad heads / n_tokens / mode");
+    const la::KvPlan p = la::kv_plan(heads, n_tokens, mode == LIN_ATTN_MODE_HIGH);
+    int most = 0;
+    for (int h = 0; h < heads; ++h) {
+        const int n = la::segments_of_head(p, h);
+        most = n > most ? n : most;
+    }
+    if (chunks) *chunks = p.chunks;
+    if (max_segments) *max_segments = most;
+    return ok();
 }
 
 int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int head_dim, int device) {
@@ -274,9 +274,9 @@ int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int h
     c->max_tokens = max_tokens;
     c->head_dim = head_dim;
     c->n_sms = sms;
-    c->splits_alloc = splits_bound(heads, max_tokens);
+    c->seg_stride_alloc = la::kv_seg_stride_bound(heads);
     const size_t dd = static_cast<size_t>(head_dim) * head_dim;
-    bool good = cudaMalloc(&c->partial, sizeof(float) * dd * heads * c->splits_alloc) == cudaSuccess &&
+    bool good = cudaMalloc(&c->partial, sizeof(float) * dd * heads * c->seg_stride_alloc) == cudaSuccess &&
                 cudaMalloc(&c->kv, sizeof(float) * dd * heads) == cudaSuccess &&
                 cudaMalloc(&c->kv_image, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads) == cudaSuccess &&
                 cudaMalloc(&c->status, sizeof(int)) == cudaSuccess;

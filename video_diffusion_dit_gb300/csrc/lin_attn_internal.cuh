@@ -7,34 +7,77 @@
 
 namespace la {
 
-// Token tile of the tensor-core KV partial kernel (rows per pipeline stage).
+// Token tile of the KV reduction (rows per pipeline stage of the tensor-core kernel, and
+// the unit of the work split).
 constexpr int kKvTile = 64;
 // Token tile of the tensor-core apply kernel (MMA M).
 constexpr int kApplyTile = 128;
-// Upper bound on token splits per head (the reduction keeps one FP32 value per split in
-// registers).
-constexpr int kMaxSplits = 64;
-// Target number of (head, split) work units of the KV partial kernel: a constant chosen
-// for a 152-SM part, so the split plan - and with it the summation order - is fixed by
-// the shape alone.
-constexpr int kSplitUnitsTarget = 760;
+// Work chunks of the KV reduction.  The layer's (head, 64-token tile) sequence, heads
+// outermost, is cut into G equal contiguous chunks; each chunk is summed by one CTA and
+// leaves one partial KV per head it touches.  G is a constant of the kernel (152 = one
+// chunk per SM of a 152-SM part for the tensor-core kernel, four per SM for the CUDA-core
+// kernel), never read from the device, so the summation order is fixed by the shape.
+constexpr int kChunksTensorCore = 152;
+constexpr int kChunksCudaCore = 608;
+constexpr int kChunksPerHeadCap = 150;  // G <= 150 * H keeps a head under kMaxSegments partials
+constexpr int kMaxSegments = 160;       // partials per head the reduction can add
 
-struct SplitPlan {
-    int splits;     // S: splits per head
-    int64_t chunk;  // tokens per split (multiple of kKvTile); the last split may be shorter
+struct KvPlan {
+    int64_t tiles_per_head;  // ceil(N / kKvTile)
+    int64_t total_tiles;     // H * tiles_per_head
+    int chunks;              // G
+    int seg_stride;          // partial slots per head: ceil(G / H) + 1 >= segments of any head
 };
 
-__host__ __device__ inline SplitPlan split_plan(int heads, int64_t n_tokens) {
-    int s0 = (kSplitUnitsTarget + heads - 1) / heads;
-    if (s0 < 1) s0 = 1;
-    if (s0 > kMaxSplits) s0 = kMaxSplits;
-    int64_t per = (n_tokens + s0 - 1) / s0;
-    int64_t chunk = ((per + kKvTile - 1) / kKvTile) * kKvTile;
-    if (chunk < kKvTile) chunk = kKvTile;
-    SplitPlan p;
-    p.chunk = chunk;
-    p.splits = static_cast<int>((n_tokens + chunk - 1) / chunk);
+__host__ __device__ inline KvPlan kv_plan(int heads, int64_t n_tokens, bool tensor_cores) {
+    KvPlan p;
+    p.tiles_per_head = (n_tokens + kKvTile - 1) / kKvTile;
+    p.total_tiles = p.tiles_per_head * heads;
+    int64_t g = tensor_cores ? kChunksTensorCore : kChunksCudaCore;
+    if (g > p.total_tiles) g = p.total_tiles;
+    if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
+    p.chunks = static_cast<int>(g);
+    p.seg_stride = (p.chunks + heads - 1) / heads + 1;
     return p;
+}
+// First tile of chunk c (chunk c covers [chunk_begin(c), chunk_begin(c + 1))).
+__host__ __device__ inline int64_t chunk_begin(const KvPlan& p, int64_t c) { return c * p.total_tiles / p.chunks; }
+// The chunk that holds tile t.
+__host__ __device__ inline int64_t chunk_of_tile(const KvPlan& p, int64_t t) {
+    return ((t + 1) * p.chunks - 1) / p.total_tiles;
+}
+// Partial slot of (head h, chunk c) and the number of partials of head h.
+__host__ __device__ inline int segment_of(const KvPlan& p, int h, int64_t c) {
+    return static_cast<int>(c - chunk_of_tile(p, h * p.tiles_per_head));
+}
+__host__ __device__ inline int segments_of_head(const KvPlan& p, int h) {
+    return static_cast<int>(chunk_of_tile(p, (h + 1) * p.tiles_per_head - 1) - chunk_of_tile(p, h * p.tiles_per_head) +
+                            1);
+}
+// Largest seg_stride any n_tokens can produce for `heads` (scratch sizing).
+__host__ __device__ inline int kv_seg_stride_bound(int heads) {
+    int64_t g = kChunksCudaCore > kChunksTensorCore ? kChunksCudaCore : kChunksTensorCore;
+    if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
+    return static_cast<int>((g + heads - 1) / heads + 1);
+}
+
+// Work of one launch of the KV reduction: heads [h0, h0 + hc) of the layer (the K/V
+// pointers and tensor maps start at head h0), i.e. tiles [t_lo, t_hi) of chunks
+// [c_lo, c_hi].
+struct KvLaunch {
+    int h0;
+    int64_t t_lo, t_hi;
+    int64_t c_lo;
+    int n_chunks;
+};
+__host__ __device__ inline KvLaunch kv_launch(const KvPlan& p, int h0, int hc) {
+    KvLaunch l;
+    l.h0 = h0;
+    l.t_lo = h0 * p.tiles_per_head;
+    l.t_hi = (h0 + hc) * p.tiles_per_head;
+    l.c_lo = chunk_of_tile(p, l.t_lo);
+    l.n_chunks = static_cast<int>(chunk_of_tile(p, l.t_hi - 1) - l.c_lo + 1);
+    return l;
 }
 
 // Number of 64-wide column blocks ("atoms") that cover the head dim: 1 for D <= 64, else 2.
@@ -49,22 +92,43 @@ __host__ __device__ inline int64_t kv_image_bytes(int head_dim) {
 // Sets the calling thread's last-error text (lin_attn_last_error); returns `code`.
 int record_error(int code, const char* msg);
 
-// ---------------------------------------------------------------- launchers
-// Each returns cudaSuccess or the launch error.
+// Launch `kernel` with programmatic stream serialisation: it may start while the previous
+// kernel of the stream finishes.  Every kernel launched this way calls grid_dependency_wait
+// before it touches memory an earlier kernel of the stream may still be using.
+template <typename... Params, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
-// KV partial sums on tensor cores (BF16 x BF16 -> FP32): partial[h][s][i][j].
-cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int heads,
-                                 int64_t n_tokens, int head_dim, SplitPlan plan, int grid, int* status,
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  `partial` is the base of the layer's
+// [H][seg_stride][D][D] partial buffer (head 0); the K/V maps/pointers start at head h0.
+
+// KV partial sums on tensor cores (BF16 x BF16 -> FP32).
+cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, int* status,
                                  cudaStream_t stream);
 
 // KV partial sums with FP32 FMA on CUDA cores (operands upcast from BF16).
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int heads,
-                                   int64_t n_tokens, int head_dim, SplitPlan plan, cudaStream_t stream);
+cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int64_t n_tokens,
+                                   int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream);
 
-// Fixed-order pairwise reduction of the split partials: kv[h][i][j] (FP32) and, if
-// kv_image != nullptr, its three-term BF16 image for the tensor-core apply.
-cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int heads, int head_dim,
-                               int splits, cudaStream_t stream);
+// Fixed-order pairwise reduction of each head's partials for heads [h0, h0 + hc):
+// kv[h][i][j] (FP32) and, if kv_image != nullptr, its three-term BF16 image for the
+// tensor-core apply.  kv / kv_image are the layer's base pointers (head 0).
+cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
+                               const KvPlan& plan, cudaStream_t stream);
 
 // out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms.
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,

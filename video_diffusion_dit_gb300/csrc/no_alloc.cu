@@ -1,6 +1,6 @@
 // lin_attn_forward_noalloc: the layer call for callers that cannot allocate device memory.
 //
-// The regular entry point keeps its scratch (per-split KV partial sums, the reduced KV,
+// The regular entry point keeps its scratch (per-chunk KV partial sums, the reduced KV,
 // the KV image the apply kernel reads, a status word) in a context made by
 // lin_attn_create, which calls cudaMalloc.  Some callers cannot do that: a plugin whose
 // host forbids allocation inside its enqueue/execute callback, a serving process whose
@@ -103,10 +103,11 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
             return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
 
     // Scratch carve-up: partials | KV | KV image | status word, each 256-byte aligned.
-    const la::SplitPlan plan = la::split_plan(heads, n_tokens);
+    const la::KvPlan plan = la::kv_plan(heads, n_tokens, mode == LIN_ATTN_MODE_HIGH);
+    const la::KvLaunch work = la::kv_launch(plan, 0, heads);
     const size_t dd = static_cast<size_t>(head_dim) * head_dim;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t partial_bytes = up(sizeof(float) * dd * heads * plan.splits);
+    const size_t partial_bytes = up(sizeof(float) * dd * heads * plan.seg_stride);
     const size_t kv_bytes = up(sizeof(float) * dd * heads);
     const size_t image_bytes = static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads;
     const size_t need = partial_bytes + kv_bytes + up(image_bytes) + 256;
@@ -150,14 +151,14 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
         if (!make_map(&tk, k_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile) ||
             !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
             return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        e = la::launch_kv_partial_tc(tk, tv, partial, heads, n_tokens, head_dim, plan, su.n_sms, status, s);
+        e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, status, s);
     } else {
         e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k_rot), static_cast<const uint16_t*>(v), partial,
-                                       heads, n_tokens, head_dim, plan, s);
+                                       n_tokens, head_dim, plan, work, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "kv_partial launch");
-    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, heads, head_dim,
-                               plan.splits, s);
+    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, 0, heads, head_dim, plan,
+                               s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (mode == LIN_ATTN_MODE_HIGH) {
         CUtensorMap tq, to;

@@ -75,6 +75,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on (the previous kernels of the stream) have
+// completed and their memory is visible.  A no-op when the grid was launched normally.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel of the stream (if launched with programmatic serialisation) to be
+// scheduled before this grid completes; it still waits for completion before consuming.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk copies
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");

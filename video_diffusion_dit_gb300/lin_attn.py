@@ -19,7 +19,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_OOM, ERR_TIM
 
 EXPORTS = (
     "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_host",
-    "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_num_splits",
+    "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
     "lin_attn_forward_noalloc",
 )
@@ -37,7 +37,7 @@ def _load():
         "lin_attn_forward_host": ([p, p, p, p, p, p, i32, i64, i32, p], i32),
         "lin_attn_debug_kv": ([p, p, p], i32),
         "lin_attn_device_status": ([p, p], i32),
-        "lin_attn_num_splits": ([i32, i64, i32], i32),
+        "lin_attn_kv_plan": ([i32, i64, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "lin_attn_set_stage_events": ([p, ctypes.POINTER(p), i32], i32),
         "lin_attn_error_string": ([i32], ctypes.c_char_p),
         "lin_attn_last_error": ([], ctypes.c_char_p),
@@ -70,8 +70,11 @@ def error_string(status: int) -> str:
     return lib.lin_attn_error_string(status).decode()
 
 
-def num_splits(heads: int, n_tokens: int, head_dim: int) -> int:
-    return lib.lin_attn_num_splits(heads, n_tokens, head_dim)
+def kv_plan(heads: int, n_tokens: int, mode="high"):
+    """(chunks, max partials per head) of the KV reduction for this shape and tier."""
+    c, m = ctypes.c_int(), ctypes.c_int()
+    _check(lib.lin_attn_kv_plan(heads, n_tokens, _mode(mode), ctypes.byref(c), ctypes.byref(m)), "lin_attn_kv_plan")
+    return c.value, m.value
 
 
 def _mode(mode) -> int:
