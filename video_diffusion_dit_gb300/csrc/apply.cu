@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             // Q tiles are inputs of the call and may be fetched before the reduction that
             // produces the KV image has finished; the image is loaded only after the wait.
             bool waited = false;
+            const uint64_t pol = policy_evict_first();
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             bool ok = true, b_pending = false;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kQAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
-                    tma_load_3d(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x, n0, h);
+                    tma_load_3d_hint(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x, n0, h, pol);
                 if (h != cur_h) {
                     if (!waited) {
                         grid_dependency_wait();
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         const int q = warp & 3;
         const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
         uint32_t nstore = 0;
+        const uint64_t spol = policy_evict_first();
         constexpr int kCols = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
         const int groups = (head_dim + kCols - 1) / kCols;
         for (int t = t_begin; t < t_end; ++t) {
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(&tm_out, sbuf, kCols * g, row0, h);
+                    tma_store_3d_hint(&tm_out, sbuf, kCols * g, row0, h, spol);
                     bulk_commit();
                 }
                 ++nstore;

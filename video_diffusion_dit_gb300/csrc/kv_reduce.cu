@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: every tile of the chunk, in order
+            const uint64_t pol = policy_evict_first();
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x) {
-                    tma_load_3d(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, y, h - work.h0);
-                    tma_load_3d(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, y, h - work.h0);
+                    tma_load_3d_hint(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, y, h - work.h0, pol);
+                    tma_load_3d_hint(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, y, h - work.h0, pol);
                 }
             }
             if (!ok) {
