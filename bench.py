@@ -240,13 +240,20 @@ def run_ours(args, w, world, rank, local, dist):
     H, N, D = w.heads, w.tokens, w.head_dim
     out_dtype = torch.float32 if args.out_dtype == "f32" else torch.bfloat16
     out_bytes = 4 if out_dtype == torch.float32 else 2
-    layer = synth.make_layer(H, N, D, w.seed + rank, w.grid, device=dev)
+    # --layers L: L distinct layers with their own seeded inputs (a denoise step's worth),
+    # visited in turn, one per step.
+    layers = [synth.make_layer(H, N, D, w.seed + rank * args.layers + i, w.grid, device=dev)
+              for i in range(args.layers)]
+    layer = layers[0]
     out = torch.empty(1, H, N, D, dtype=out_dtype, device=dev)
     ctx = lin_attn.LinAttn(H, N, D, dev)
     stream = torch.cuda.current_stream(dev)
+    counter = [0]
 
     def step():
-        ctx.forward(layer["q_rot"], layer["k_rot"], layer["v"], layer["den"], out=out, mode=args.mode, stream=stream)
+        g = layers[counter[0] % len(layers)]
+        counter[0] += 1
+        ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -316,6 +323,7 @@ def run_ours(args, w, world, rank, local, dist):
                 "workload": f"{w.name} layer: H={H}, N={N}, D={D}", "mode": args.mode, "out_dtype": args.out_dtype,
                 "accumulate": "f32", "l2": "inputs larger than L2 (no flush needed)",
                 "bytes_per_call": nbytes["total"], "parallelism": f"replicas x{world}",
+                "layers": args.layers,
             },
             "achieved_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
             "stage_ms": stage_ms,
@@ -344,6 +352,7 @@ def main():
     ap.add_argument("--mode", default="high", choices=["high", "lossless"])
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=1, help="distinct seeded layers visited in turn, one per step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

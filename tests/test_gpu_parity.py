@@ -126,6 +126,48 @@ def test_full_size_sampled(la, dev, name):
                 assert kv_err <= KV_TOL, f"{name} {mode}: KV rel-L2 {kv_err:.3e}"
 
 
+@pytest.mark.parametrize("n", synth.SWEEP_TOKENS)
+def test_token_sweep_sampled(la, dev, n):
+    """The N sweep at H=20, D=112 and at H=32, D=64: KV whole, output on sampled rows."""
+    for name in (f"sweep_n{n}", f"sweep_n{n}_d64"):
+        w = synth.WORKLOADS[name]
+        H, N, D = w.heads, w.tokens, w.head_dim
+        layer = synth.make_workload(w, device=dev)
+        qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+        kv_ref = oracle.kv(kb, vb)
+        rows = sampled_rows(H, N, 2048, n)
+        ref = oracle.apply_rows(qb, kv_ref, den, rows)
+        with la.LinAttn(H, N, D, dev) as ctx:
+            for mode in MODES:
+                out = run(ctx, layer, mode, torch.float32)
+                got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+                assert rel_l2(got, ref) <= TOL[torch.float32], (name, mode)
+                assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= KV_TOL, (name, mode)
+
+
+def test_denoise_step_twenty_layers(la, dev):
+    """20 sequential layer calls at the 720p shape with fresh seeded inputs per layer on one
+    context (the scratch is reused call after call); the first and last layers are held to
+    the oracle on sampled rows, every call must finish with a clean status."""
+    w = synth.WORKLOADS["720p_193f"]
+    H, N, D = w.heads, w.tokens, w.head_dim
+    out = torch.empty(1, H, N, D, device=dev)
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in MODES:
+            for layer_idx in range(synth.DENOISE_LAYERS):
+                layer = synth.make_layer(H, N, D, seed=layer_idx, grid=w.grid, device=dev)
+                ctx.forward(layer["q_rot"], layer["k_rot"], layer["v"], layer["den"], out=out, mode=mode)
+                if layer_idx in (0, synth.DENOISE_LAYERS - 1):
+                    assert ctx.device_status() == 0
+                    qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+                    kv_ref = oracle.kv(kb, vb)
+                    rows = sampled_rows(H, N, 1024, layer_idx)
+                    ref = oracle.apply_rows(qb, kv_ref, den, rows)
+                    got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+                    assert rel_l2(got, ref) <= TOL[torch.float32], (mode, layer_idx)
+            assert ctx.device_status() == 0
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_bitwise_deterministic(la, dev, mode):
     w = synth.WORKLOADS["480p_81f"]

@@ -253,8 +253,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 // ============================================================================ CUDA cores
 // 'lossless': both operands upcast from BF16 to FP32 (exact), FP32 FMA.  One CTA per chunk;
 // thread (ti, tj) owns KV rows ti + 16a and columns tj + 16b of the running segment sum;
-// tokens are added in ascending order, 32 at a time through shared memory.
+// tokens are added in ascending order, 32 at a time through shared memory, into a sum
+// that is folded into the segment total every 256 tokens.
 constexpr int kFfmaKvRows = 32;
+constexpr int kFfmaPromoteRows = 256;
 
 template <int C>
 __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __restrict__ k,
@@ -276,13 +278,24 @@ __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __
         const uint16_t* kh = k + static_cast<int64_t>(h - work.h0) * n_tokens * D;
         const uint16_t* vh = v + static_cast<int64_t>(h - work.h0) * n_tokens * D;
 
-        float acc[C][C];
+        // Two-level FP32 sum: `acc` runs over at most kFfmaPromoteRows tokens, then is
+        // added into the segment total `tot` (keeps the rounding error of long segments down).
+        float acc[C][C], tot[C][C];
 #pragma unroll
         for (int a = 0; a < C; ++a)
 #pragma unroll
-            for (int b = 0; b < C; ++b) acc[a][b] = 0.f;
+            for (int b = 0; b < C; ++b) acc[a][b] = tot[a][b] = 0.f;
 
         for (int n0 = n_begin; n0 < n_end; n0 += kFfmaKvRows) {
+            if (n0 != n_begin && (n0 - n_begin) % kFfmaPromoteRows == 0) {
+#pragma unroll
+                for (int a = 0; a < C; ++a)
+#pragma unroll
+                    for (int b = 0; b < C; ++b) {
+                        tot[a][b] += acc[a][b];
+                        acc[a][b] = 0.f;
+                    }
+            }
             const int rows = min(kFfmaKvRows, n_end - n0);
             __syncthreads();
             for (int idx = threadIdx.x; idx < kFfmaKvRows * (D / 8); idx += 256) {
@@ -320,7 +333,7 @@ __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __
 #pragma unroll
         for (int a = 0; a < C; ++a)
 #pragma unroll
-            for (int b = 0; b < C; ++b) dst[(ti + 16 * a) * D + tj + 16 * b] = acc[a][b];
+            for (int b = 0; b < C; ++b) dst[(ti + 16 * a) * D + tj + 16 * b] = tot[a][b] + acc[a][b];
         t = seg_end;
     }
 }

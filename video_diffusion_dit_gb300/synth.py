@@ -55,11 +55,13 @@ WORKLOADS = {
     "720p_193f": Workload("720p_193f", 20, 180320, 112, (49, 46, 80)),
     "720p_193f_d64": Workload("720p_193f_d64", 32, 180320, 64, (49, 46, 80)),
 }
-
-
-def sweep_workload(tokens: int, heads: int = 20, head_dim: int = 112, seed: int = 0) -> Workload:
-    """A point of the token-count sweep (1-D positions)."""
-    return Workload(f"sweep_n{tokens}_h{heads}_d{head_dim}", heads, tokens, head_dim, None, seed)
+# Token-count sweep at the 720p head shape (powers of two, 1-D positions).
+SWEEP_TOKENS = tuple(1 << k for k in range(12, 19))  # 4096 .. 262144
+for _n in SWEEP_TOKENS:
+    WORKLOADS[f"sweep_n{_n}"] = Workload(f"sweep_n{_n}", 20, _n, 112, None)
+    WORKLOADS[f"sweep_n{_n}_d64"] = Workload(f"sweep_n{_n}_d64", 32, _n, 64, None)
+# A denoise step touches this many linear-attention layers, each with its own inputs.
+DENOISE_LAYERS = 20
 
 
 def _axis_chunks(head_dim: int, grid) -> list[tuple[int, int]]:
