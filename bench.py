@@ -244,6 +244,10 @@ def run_ours(args, w, world, rank, local, dist):
     # visited in turn, one per step.
     layers = [synth.make_layer(H, N, D, w.seed + rank * args.layers + i, w.grid, device=dev)
               for i in range(args.layers)]
+    if args.layout == "nhd":  # the model's [1, N, H, D] projection layout
+        for g in layers:
+            for key in ("q_rot", "k_rot", "v"):
+                g[key] = g[key].permute(0, 2, 1, 3).contiguous()
     layer = layers[0]
     out = torch.empty(1, H, N, D, dtype=out_dtype, device=dev)
     ctx = lin_attn.LinAttn(H, N, D, dev)
@@ -253,7 +257,8 @@ def run_ours(args, w, world, rank, local, dist):
     def step():
         g = layers[counter[0] % len(layers)]
         counter[0] += 1
-        ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream)
+        ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream,
+                    layout=args.layout)
 
     for _ in range(args.warmup):
         step()
@@ -291,7 +296,9 @@ def run_ours(args, w, world, rank, local, dist):
     stage_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                 for j, name in enumerate(("kv_partial", "kv_finalize", "apply"))}
 
-    # ---- end to end through the host-buffer entry point (pinned host memory)
+    # ---- end to end through the host-buffer entry point (pinned host memory, [1, H, N, D])
+    if args.layout == "nhd":
+        layer = {k: (t.permute(0, 2, 1, 3).contiguous() if k != "den" else t) for k, t in layer.items()}
     host = {k: t.cpu().pin_memory() for k, t in layer.items()}
     hout = torch.empty(1, H, N, D, dtype=out_dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -321,9 +328,10 @@ def run_ours(args, w, world, rank, local, dist):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {
                 "workload": f"{w.name} layer: H={H}, N={N}, D={D}", "mode": args.mode, "out_dtype": args.out_dtype,
-                "accumulate": "f32", "l2": "inputs larger than L2 (no flush needed)",
+                "accumulate": "f32",
+                "l2": "inputs larger than L2; consecutive steps use different layers' inputs (no flush needed)",
                 "bytes_per_call": nbytes["total"], "parallelism": f"replicas x{world}",
-                "layers": args.layers,
+                "layers": args.layers, "layout": args.layout,
             },
             "achieved_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
             "stage_ms": stage_ms,
@@ -352,7 +360,10 @@ def main():
     ap.add_argument("--mode", default="high", choices=["high", "lossless"])
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--layers", type=int, default=1, help="distinct seeded layers visited in turn, one per step")
+    ap.add_argument("--layers", type=int, default=2,
+                    help="distinct seeded layers visited in turn, one per step (2: no step finds the previous "
+                         "step's data in L2)")
+    ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"], help="activation layout of the timed calls")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

@@ -53,6 +53,10 @@ typedef struct lin_attn_ctx lin_attn_ctx;
 
 enum lin_attn_mode { LIN_ATTN_MODE_HIGH = 0, LIN_ATTN_MODE_LOSSLESS = 1 };
 enum lin_attn_out_dtype { LIN_ATTN_OUT_F32 = 0, LIN_ATTN_OUT_BF16 = 1 };
+enum lin_attn_layout {
+    LIN_ATTN_LAYOUT_HND = 0, /* q_rot, k_rot, v, out: [1, H, N, D] (each head one N x D block)  */
+    LIN_ATTN_LAYOUT_NHD = 1  /* q_rot, k_rot, v: [1, N, H, D]; out: [1, N, H*D] (token-major)   */
+};
 
 enum lin_attn_status {
     LIN_ATTN_OK = 0,
@@ -92,6 +96,19 @@ int lin_attn_destroy(lin_attn_ctx *ctx);
 int lin_attn_forward(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
                      const float *normalizer, void *out, int out_dtype, int64_t n_tokens,
                      int mode, struct CUstream_st *stream);
+
+/*
+ * lin_attn_forward with a choice of activation layout.  LIN_ATTN_LAYOUT_NHD reads Q_rot,
+ * K_rot, V as [1, N, H, D] - the per-head views of the model's packed projection output,
+ * before the page's permute to [B, H, D, N] (page 1, 关键源码片段, `sana_video.py`:
+ * `.view(batch_size, sequence_length, num_heads, head_dim)`) - and writes out as
+ * [1, N, H*D], the `flatten(1, 2).transpose(1, 2)` form the output projection consumes.
+ * The normaliser stays [1, H, N, 1] (the page's [B, H, 1, N]).  Same numbers as the
+ * head-major call (bitwise); LIN_ATTN_LAYOUT_HND is exactly lin_attn_forward.
+ */
+int lin_attn_forward_layout(lin_attn_ctx *ctx, const void *q_rot, const void *k_rot, const void *v,
+                            const float *normalizer, void *out, int out_dtype, int64_t n_tokens,
+                            int mode, int layout, struct CUstream_st *stream);
 
 /*
  * Same layer call on HOST buffers (same shapes and dtypes, any alignment).  Copies the

@@ -285,3 +285,30 @@ def test_ragged_tail_stores_repeated(la, dev, N):
             assert err <= TOL[dt], f"N={N} {dt}: rel-L2 {err:.3e}"
             for _ in range(8):
                 assert torch.equal(run(ctx, g, "high", dt), first)
+
+
+def to_token_major(t):
+    """[1, H, N, D] -> contiguous [1, N, H, D]."""
+    return t.permute(0, 2, 1, 3).contiguous()
+
+
+@pytest.mark.parametrize("shape", [(20, 3001, 112), (3, 777, 64), (2, 256, 32), (5, 129, 128)])
+def test_token_major_layout(la, dev, shape):
+    """The page-native layout: [1, N, H, D] activations in, [1, N, H*D] out.  Same numbers as
+    the head-major call, bitwise, in both tiers and output types; checked against the oracle."""
+    H, N, D = shape
+    layer = synth.make_layer(H, N, D, seed=N)
+    qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
+    ref = oracle.forward(qb, kb, vb, den)
+    g = to_dev(layer, dev)
+    tm = {k: to_token_major(g[k]) for k in ("q_rot", "k_rot", "v")}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in MODES:
+            for dt in (torch.float32, torch.bfloat16):
+                hm = run(ctx, g, mode, dt)
+                out = ctx.forward(tm["q_rot"], tm["k_rot"], tm["v"], g["den"], mode=mode, out_dtype=dt, layout="nhd")
+                assert ctx.device_status() == 0
+                assert tuple(out.shape) == (1, N, H * D)
+                assert torch.equal(out.view(1, N, H, D), to_token_major(hm)), (mode, dt)
+                err = rel_l2(out.view(N, H, D).permute(1, 0, 2).double().cpu().numpy(), ref)
+                assert err <= TOL[dt], (mode, dt, err)

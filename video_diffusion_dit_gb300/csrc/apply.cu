@@ -39,7 +39,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kApplyThreads, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                     const uint8_t* __restrict__ kv_image, const float* __restrict__ den, int heads, int n_tokens,
-                    int head_dim, int tiles_per_head, int* status) {
+                    int head_dim, int tiles_per_head, int token_major, int* status) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kQAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
-                    tma_load_3d_hint(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x, n0, h, pol);
+                    tma_load_3d_hint(q_smem + (st * NBOX + x) * kQAtomBytes, &tm_q, q_full0 + 8u * st, 64 * x,
+                                     token_major ? h : n0, token_major ? n0 : h, pol);
                 if (h != cur_h) {
                     if (!waited) {
                         grid_dependency_wait();
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d_hint(&tm_out, sbuf, kCols * g, row0, h, spol);
+                    tma_store_3d_hint(&tm_out, sbuf, kCols * g, token_major ? h : row0, token_major ? row0 : h, spol);
                     bulk_commit();
                 }
                 ++nstore;
@@ -278,9 +279,10 @@ __host__ __device__ inline size_t apply_ffma_smem_bytes(int head_dim) {
 }
 
 template <int C, bool OUT_BF16>
-__global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restrict__ q, const float* __restrict__ kv,
-                                                         const float* __restrict__ den, void* __restrict__ out,
-                                                         int heads, int n_tokens, int tiles_per_head) {
+__global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restrict__ q, const Strides sd,
+                                                         const float* __restrict__ kv, const float* __restrict__ den,
+                                                         void* __restrict__ out, int heads, int n_tokens,
+                                                         int tiles_per_head) {
     constexpr int D = 16 * C;
     extern __shared__ float sm[];
     float* kvs = sm;           // [D][D]
@@ -294,7 +296,8 @@ __global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restr
         const int h = t / tiles_per_head;
         const int n0 = (t % tiles_per_head) * kFfmaTile;
         const int rows = min(kFfmaTile, n_tokens - n0);
-        const int64_t row_base = static_cast<int64_t>(h) * n_tokens + n0;
+        const int64_t row_base = static_cast<int64_t>(h) * n_tokens + n0;    // den index of row 0
+        const int64_t elem_base = h * sd.head + static_cast<int64_t>(n0) * sd.token;  // Q / out offset of row 0
         __syncthreads();
         if (h != cur_h) {
             const float4* src = reinterpret_cast<const float4*>(kv + static_cast<int64_t>(h) * D * D);
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restr
         for (int idx = threadIdx.x; idx < kFfmaTile * (D / 8); idx += 256) {
             const int r = idx % kFfmaTile, c = idx / kFfmaTile;
             uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < rows) w = *reinterpret_cast<const uint4*>(q + (row_base + r) * D + 8 * c);
+            if (r < rows) w = *reinterpret_cast<const uint4*>(q + elem_base + r * sd.token + 8 * c);
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -342,14 +345,18 @@ __global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restr
         }
         __syncthreads();
         if (!OUT_BF16) {
-            float* o = reinterpret_cast<float*>(out) + row_base * D;
-            for (int idx = threadIdx.x; idx < rows * D; idx += 256) o[idx] = ys[(idx / D) * (D + 1) + idx % D];
+            float* o = reinterpret_cast<float*>(out) + elem_base;
+            for (int idx = threadIdx.x; idx < rows * D; idx += 256) {
+                const int r = idx / D, c = idx % D;
+                o[r * sd.token + c] = ys[r * (D + 1) + c];
+            }
         } else {
-            __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + row_base * D);
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + elem_base;
             for (int idx = threadIdx.x; idx < rows * D / 2; idx += 256) {
                 const int e = 2 * idx;
                 const int r = e / D, c = e % D;
-                o[idx] = __floats2bfloat162_rn(ys[r * (D + 1) + c], ys[r * (D + 1) + c + 1]);
+                *reinterpret_cast<__nv_bfloat162*>(o + r * sd.token + c) =
+                    __floats2bfloat162_rn(ys[r * (D + 1) + c], ys[r * (D + 1) + c + 1]);
             }
         }
     }
@@ -357,19 +364,20 @@ __global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restr
 
 template <int NBOX, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
-                      int heads, int n_tokens, int head_dim, int grid, int* status, cudaStream_t stream) {
+                      int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
+                      cudaStream_t stream) {
     const uint32_t smem = apply_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
     return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
-                             img, den, heads, n_tokens, head_dim, tph, status);
+                             img, den, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status);
 }
 
 template <int C, bool BF16>
-cudaError_t launch_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads, int n_tokens,
-                        int grid, cudaStream_t stream) {
+cudaError_t launch_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
+                        int n_tokens, int grid, cudaStream_t stream) {
     const size_t smem = apply_ffma_smem_bytes(16 * C);
     cudaError_t e = cudaFuncSetAttribute(apply_ffma_kernel<C, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -377,22 +385,22 @@ cudaError_t launch_ffma(const uint16_t* q, const float* kv, const float* den, vo
     const int tph = (n_tokens + kFfmaTile - 1) / kFfmaTile;
     const int total = heads * tph;
     if (grid > total) grid = total;
-    apply_ffma_kernel<C, BF16><<<grid, 256, smem, stream>>>(q, kv, den, out, heads, n_tokens, tph);
+    apply_ffma_kernel<C, BF16><<<grid, 256, smem, stream>>>(q, sd, kv, den, out, heads, n_tokens, tph);
     return cudaGetLastError();
 }
 
 template <bool BF16>
-cudaError_t dispatch_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads, int n_tokens,
-                          int head_dim, int grid, cudaStream_t stream) {
+cudaError_t dispatch_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
+                          int n_tokens, int head_dim, int grid, cudaStream_t stream) {
     switch (head_dim / 16) {
-        case 1: return launch_ffma<1, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 2: return launch_ffma<2, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 3: return launch_ffma<3, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 4: return launch_ffma<4, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 5: return launch_ffma<5, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 6: return launch_ffma<6, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 7: return launch_ffma<7, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
-        case 8: return launch_ffma<8, BF16>(q, kv, den, out, heads, n_tokens, grid, stream);
+        case 1: return launch_ffma<1, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 2: return launch_ffma<2, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 3: return launch_ffma<3, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 4: return launch_ffma<4, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 5: return launch_ffma<5, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 6: return launch_ffma<6, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 7: return launch_ffma<7, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
+        case 8: return launch_ffma<8, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -400,24 +408,24 @@ cudaError_t dispatch_ffma(const uint16_t* q, const float* kv, const float* den, 
 }  // namespace
 
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
-                            const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16, int grid,
-                            int* status, cudaStream_t stream) {
+                            const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
+                            bool token_major, int grid, int* status, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
     const int total = heads * ((n + kApplyTile - 1) / kApplyTile);
     if (grid > total) grid = total;
     const bool one = head_dim_atoms(head_dim) == 1;
     if (one)
-        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream)
-                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream);
-    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream)
-                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, grid, status, stream);
+        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
+                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
+    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
+                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
 }
 
-cudaError_t launch_apply_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads,
+cudaError_t launch_apply_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
                               int64_t n_tokens, int head_dim, bool out_bf16, int grid, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
-    return out_bf16 ? dispatch_ffma<true>(q, kv, den, out, heads, n, head_dim, grid, stream)
-                    : dispatch_ffma<false>(q, kv, den, out, heads, n, head_dim, grid, stream);
+    return out_bf16 ? dispatch_ffma<true>(q, sd, kv, den, out, heads, n, head_dim, grid, stream)
+                    : dispatch_ffma<false>(q, sd, kv, den, out, heads, n, head_dim, grid, stream);
 }
 
 }  // namespace la

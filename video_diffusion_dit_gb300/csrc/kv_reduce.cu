@@ -53,7 +53,7 @@ template <int NBOX>
 __global__ void __launch_bounds__(kKvThreads, 1)
     kv_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          float* __restrict__ partial, int head_dim, const KvPlan plan, const KvLaunch work,
-                         int* status) {
+                         int token_major, int* status) {
     using L = KvLayout<NBOX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
                 const int h = static_cast<int>(t / tph);
                 const int y = static_cast<int>((t % tph) * kKvTile);
+                const int c1 = token_major ? h - work.h0 : y, c2 = token_major ? y : h - work.h0;
                 const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
                 if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
                     ok = false;
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x) {
-                    tma_load_3d_hint(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, y, h - work.h0, pol);
-                    tma_load_3d_hint(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, y, h - work.h0, pol);
+                    tma_load_3d_hint(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, c1, c2, pol);
+                    tma_load_3d_hint(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, c1, c2, pol);
                 }
             }
             if (!ok) {
@@ -260,7 +261,7 @@ constexpr int kFfmaPromoteRows = 256;
 
 template <int C>
 __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __restrict__ k,
-                                                              const uint16_t* __restrict__ v,
+                                                              const uint16_t* __restrict__ v, const Strides sd,
                                                               float* __restrict__ partial, int n_tokens,
                                                               const KvPlan plan, const KvLaunch work) {
     constexpr int D = 16 * C;
@@ -275,8 +276,8 @@ __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __
         const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
         const int n_begin = static_cast<int>((t % tph) * kKvTile);
         const int n_end = static_cast<int>(min(static_cast<int64_t>(n_tokens), (seg_end - h * tph) * kKvTile));
-        const uint16_t* kh = k + static_cast<int64_t>(h - work.h0) * n_tokens * D;
-        const uint16_t* vh = v + static_cast<int64_t>(h - work.h0) * n_tokens * D;
+        const uint16_t* kh = k + static_cast<int64_t>(h - work.h0) * sd.head;
+        const uint16_t* vh = v + static_cast<int64_t>(h - work.h0) * sd.head;
 
         // Two-level FP32 sum: `acc` runs over at most kFfmaPromoteRows tokens, then is
         // added into the segment total `tot` (keeps the rounding error of long segments down).
@@ -302,8 +303,8 @@ __global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __
                 const int r = idx / (D / 8), c = idx % (D / 8);
                 uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
                 if (r < rows) {
-                    kw = *reinterpret_cast<const uint4*>(kh + static_cast<int64_t>(n0 + r) * D + 8 * c);
-                    vw = *reinterpret_cast<const uint4*>(vh + static_cast<int64_t>(n0 + r) * D + 8 * c);
+                    kw = *reinterpret_cast<const uint4*>(kh + static_cast<int64_t>(n0 + r) * sd.token + 8 * c);
+                    vw = *reinterpret_cast<const uint4*>(vh + static_cast<int64_t>(n0 + r) * sd.token + 8 * c);
                 }
                 const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
                 const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
@@ -439,44 +440,45 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
 
 template <int NBOX>
 cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int head_dim,
-                      const KvPlan& plan, const KvLaunch& work, int* status, cudaStream_t stream) {
+                      const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, cudaStream_t stream) {
     using L = KvLayout<NBOX>;
     cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::smem_bytes);
     if (e != cudaSuccess) return e;
     return launch_overlapped(kv_partial_tc_kernel<NBOX>, dim3(work.n_chunks), dim3(kKvThreads), L::smem_bytes, stream,
-                             tm_k, tm_v, partial, head_dim, plan, work, status);
+                             tm_k, tm_v, partial, head_dim, plan, work, token_major ? 1 : 0, status);
 }
 
 template <int C>
-cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, float* partial, int n_tokens, const KvPlan& plan,
-                        const KvLaunch& work, cudaStream_t stream) {
-    kv_partial_ffma_kernel<C><<<work.n_chunks, 256, 0, stream>>>(k, v, partial, n_tokens, plan, work);
+cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float* partial, int n_tokens,
+                        const KvPlan& plan, const KvLaunch& work, cudaStream_t stream) {
+    kv_partial_ffma_kernel<C><<<work.n_chunks, 256, 0, stream>>>(k, v, sd, partial, n_tokens, plan, work);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
-                                 int head_dim, const KvPlan& plan, const KvLaunch& work, int* status,
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
                                  cudaStream_t stream) {
     (void)n_tokens;
-    if (head_dim_atoms(head_dim) == 1) return launch_tc<1>(tm_k, tm_v, partial, head_dim, plan, work, status, stream);
-    return launch_tc<2>(tm_k, tm_v, partial, head_dim, plan, work, status, stream);
+    if (head_dim_atoms(head_dim) == 1)
+        return launch_tc<1>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream);
+    return launch_tc<2>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream);
 }
 
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int64_t n_tokens,
+cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float* partial, int64_t n_tokens,
                                    int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
     switch (head_dim / 16) {
-        case 1: return launch_ffma<1>(k, v, partial, n, plan, work, stream);
-        case 2: return launch_ffma<2>(k, v, partial, n, plan, work, stream);
-        case 3: return launch_ffma<3>(k, v, partial, n, plan, work, stream);
-        case 4: return launch_ffma<4>(k, v, partial, n, plan, work, stream);
-        case 5: return launch_ffma<5>(k, v, partial, n, plan, work, stream);
-        case 6: return launch_ffma<6>(k, v, partial, n, plan, work, stream);
-        case 7: return launch_ffma<7>(k, v, partial, n, plan, work, stream);
-        case 8: return launch_ffma<8>(k, v, partial, n, plan, work, stream);
+        case 1: return launch_ffma<1>(k, v, sd, partial, n, plan, work, stream);
+        case 2: return launch_ffma<2>(k, v, sd, partial, n, plan, work, stream);
+        case 3: return launch_ffma<3>(k, v, sd, partial, n, plan, work, stream);
+        case 4: return launch_ffma<4>(k, v, sd, partial, n, plan, work, stream);
+        case 5: return launch_ffma<5>(k, v, sd, partial, n, plan, work, stream);
+        case 6: return launch_ffma<6>(k, v, sd, partial, n, plan, work, stream);
+        case 7: return launch_ffma<7>(k, v, sd, partial, n, plan, work, stream);
+        case 8: return launch_ffma<8>(k, v, sd, partial, n, plan, work, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -90,16 +90,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D map over a contiguous [H][N][D] tensor: dim 0 = D (innermost), 1 = N, 2 = H, with a
-// (box_x, box_y, 1) box and 128-byte swizzle; out-of-range elements read as zero and are
-// skipped on stores.
+// 3-D map over a [.., N, .., D] activation of `h` heads with 128-byte swizzle; out-of-range
+// elements read as zero and are skipped on stores.  Head-major ([H][N][D], `heads_total`
+// unused): dims (D, N, H), box (box_x, rows, 1).  Token-major ([N][heads_total][D], the map
+// covering `h` heads from `base`): dims (D, H, N), box (box_x, 1, rows).
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t d, int64_t n,
-             int64_t h, uint32_t box_x, uint32_t box_y) {
+             int64_t h, uint32_t box_x, uint32_t box_y, bool token_major = false, int64_t heads_total = 0) {
     auto fn = encode_fn();
     if (!fn) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(h)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes), static_cast<cuuint64_t>(n * d * elem_bytes)};
     cuuint32_t box[3] = {box_x, box_y, 1};
+    if (token_major) {
+        dims[1] = static_cast<cuuint64_t>(h);
+        dims[2] = static_cast<cuuint64_t>(n);
+        strides[0] = static_cast<cuuint64_t>(d * elem_bytes);
+        strides[1] = static_cast<cuuint64_t>(heads_total * d * elem_bytes);
+        box[1] = 1;
+        box[2] = box_y;
+    }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -143,52 +152,54 @@ int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void
 // brackets the stages.
 int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
                   int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream, int h0, int hc,
-                  cudaEvent_t* ev) {
+                  cudaEvent_t* ev, int layout = LIN_ATTN_LAYOUT_HND) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
     const bool tc = mode == LIN_ATTN_MODE_HIGH;
+    const bool tm = layout == LIN_ATTN_LAYOUT_NHD;  // token-major activations
     const la::KvPlan plan = la::kv_plan(H, n_tokens, tc);
     const la::KvLaunch work = la::kv_launch(plan, h0, hc);
-    const size_t head_elems = static_cast<size_t>(n_tokens) * D;
+    const la::Strides sd = tm ? la::Strides{D, static_cast<int64_t>(H) * D}
+                              : la::Strides{static_cast<int64_t>(n_tokens) * D, D};
     const size_t dd = static_cast<size_t>(D) * D;
-    q = static_cast<const uint16_t*>(q) + h0 * head_elems;
-    k = static_cast<const uint16_t*>(k) + h0 * head_elems;
-    v = static_cast<const uint16_t*>(v) + h0 * head_elems;
+    q = static_cast<const uint16_t*>(q) + h0 * sd.head;
+    k = static_cast<const uint16_t*>(k) + h0 * sd.head;
+    v = static_cast<const uint16_t*>(v) + h0 * sd.head;
     den += h0 * static_cast<size_t>(n_tokens);
-    out = static_cast<uint8_t*>(out) + h0 * head_elems * (bf16_out ? 2 : 4);
+    out = static_cast<uint8_t*>(out) + h0 * sd.head * (bf16_out ? 2 : 4);
     float* kv_h0 = c->kv + h0 * dd;
     uint8_t* image_h0 = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
     cudaError_t e;
 
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (mode == LIN_ATTN_MODE_HIGH) {
+    if (tc) {
         CUtensorMap tk, tv;
-        int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile);
+        int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile, tm, H);
         if (rc) return rc;
-        rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile);
+        rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile, tm, H);
         if (rc) return rc;
-        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, c->status, stream);
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
     } else {
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), c->partial,
-                                       n_tokens, D, plan, work, stream);
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), sd,
+                                       c->partial, n_tokens, D, plan, work, stream);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     e = la::launch_kv_finalize(c->partial, c->kv, tc ? c->kv_image : nullptr, h0, hc, D, plan, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (mode == LIN_ATTN_MODE_HIGH) {
+    if (tc) {
         CUtensorMap tq, to;
-        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile);
+        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
         if (rc) return rc;
-        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32)
-                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32);
+        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
+                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
         if (rc) return rc;
-        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream);
+        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     } else {
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), kv_h0, den, out, hc, n_tokens, D, bf16_out,
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), sd, kv_h0, den, out, hc, n_tokens, D, bf16_out,
                                   2 * c->n_sms, stream);
         if (e != cudaSuccess) return cuda_fail(e, "apply_ffma launch");
     }
@@ -319,6 +330,23 @@ int lin_attn_forward(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, co
     ctx->n_events = 0;
     return enqueue_heads(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
                          reinterpret_cast<cudaStream_t>(stream), 0, ctx->heads, ev);
+}
+
+int lin_attn_forward_layout(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,
+                            const float* normalizer, void* out, int out_dtype, int64_t n_tokens, int mode, int layout,
+                            struct CUstream_st* stream) {
+    int rc = check_call(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    if (layout != LIN_ATTN_LAYOUT_HND && layout != LIN_ATTN_LAYOUT_NHD)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "layout=%d is not LIN_ATTN_LAYOUT_HND/NHD", layout);
+    if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(normalizer) || !aligned16(out))
+        return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    cudaEvent_t* ev = ctx->n_events == 4 ? ctx->events : nullptr;
+    ctx->n_events = 0;
+    return enqueue_heads(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
+                         reinterpret_cast<cudaStream_t>(stream), 0, ctx->heads, ev, layout);
 }
 
 int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,

@@ -80,6 +80,14 @@ __host__ __device__ inline KvLaunch kv_launch(const KvPlan& p, int h0, int hc) {
     return l;
 }
 
+// Element strides of a [.., N, .., D] activation (Q, K, V or out): row n of head h starts
+// at h * head + n * token.  Head-major [1, H, N, D]: (N*D, D).  Token-major [1, N, H, D],
+// the projection layout of the model: (D, H*D).
+struct Strides {
+    int64_t head;
+    int64_t token;
+};
+
 // Number of 64-wide column blocks ("atoms") that cover the head dim: 1 for D <= 64, else 2.
 __host__ __device__ inline int head_dim_atoms(int head_dim) { return (head_dim + 63) / 64; }
 
@@ -115,13 +123,14 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 // Each returns cudaSuccess or the launch error.  `partial` is the base of the layer's
 // [H][seg_stride][D][D] partial buffer (head 0); the K/V maps/pointers start at head h0.
 
-// KV partial sums on tensor cores (BF16 x BF16 -> FP32).
+// KV partial sums on tensor cores (BF16 x BF16 -> FP32).  The tensor maps index
+// (column, token, head) or, if token_major, (column, head, token).
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
-                                 int head_dim, const KvPlan& plan, const KvLaunch& work, int* status,
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
                                  cudaStream_t stream);
 
 // KV partial sums with FP32 FMA on CUDA cores (operands upcast from BF16).
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* partial, int64_t n_tokens,
+cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides st, float* partial, int64_t n_tokens,
                                    int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream);
 
 // Fixed-order pairwise reduction of each head's partials for heads [h0, h0 + hc):
@@ -130,13 +139,13 @@ cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, float* 
 cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
                                const KvPlan& plan, cudaStream_t stream);
 
-// out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms.
+// out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms (maps as above).
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
-                            const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16, int grid,
-                            int* status, cudaStream_t stream);
+                            const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
+                            bool token_major, int grid, int* status, cudaStream_t stream);
 
-// out = (Q . KV) * (1 / den) with FP32 FMA on CUDA cores.
-cudaError_t launch_apply_ffma(const uint16_t* q, const float* kv, const float* den, void* out, int heads,
+// out = (Q . KV) * (1 / den) with FP32 FMA on CUDA cores; Q and out share the strides.
+cudaError_t launch_apply_ffma(const uint16_t* q, Strides st, const float* kv, const float* den, void* out, int heads,
                               int64_t n_tokens, int head_dim, bool out_bf16, int grid, cudaStream_t stream);
 
 }  // namespace la

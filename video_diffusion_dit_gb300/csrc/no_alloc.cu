@@ -151,10 +151,11 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
         if (!make_map(&tk, k_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile) ||
             !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
             return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, status, s);
+        e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, false, status, s);
     } else {
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k_rot), static_cast<const uint16_t*>(v), partial,
-                                       n_tokens, head_dim, plan, work, s);
+        const la::Strides sd{n_tokens * head_dim, head_dim};
+        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k_rot), static_cast<const uint16_t*>(v), sd,
+                                       partial, n_tokens, head_dim, plan, work, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "kv_partial launch");
     e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, 0, heads, head_dim, plan,
@@ -169,10 +170,12 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
                                   : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, head_dim, n_tokens, heads,
                                              32, 32);
         if (!okq || !oko) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, su.n_sms, status, s);
+        e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status,
+                                s);
     } else {
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q_rot), kv, normalizer, out, heads, n_tokens, head_dim,
-                                  bf16_out, 2 * su.n_sms, s);
+        const la::Strides sd{n_tokens * head_dim, head_dim};
+        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q_rot), sd, kv, normalizer, out, heads, n_tokens,
+                                  head_dim, bf16_out, 2 * su.n_sms, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "apply launch");
     return la::record_error(LIN_ATTN_OK, "");

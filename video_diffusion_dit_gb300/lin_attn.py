@@ -14,11 +14,12 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblin_attn.so")
 
 MODE_HIGH, MODE_LOSSLESS = 0, 1
+LAYOUT_HND, LAYOUT_NHD = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(7)
 
 EXPORTS = (
-    "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_host",
+    "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_layout", "lin_attn_forward_host",
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
     "lin_attn_forward_noalloc",
@@ -34,6 +35,7 @@ def _load():
         "lin_attn_create": ([ctypes.POINTER(p), i32, i64, i32, i32], i32),
         "lin_attn_destroy": ([p], i32),
         "lin_attn_forward": ([p, p, p, p, p, p, i32, i64, i32, p], i32),
+        "lin_attn_forward_layout": ([p, p, p, p, p, p, i32, i64, i32, i32, p], i32),
         "lin_attn_forward_host": ([p, p, p, p, p, p, i32, i64, i32, p], i32),
         "lin_attn_debug_kv": ([p, p, p], i32),
         "lin_attn_device_status": ([p, p], i32),
@@ -133,15 +135,20 @@ class LinAttn:
         self._h = h
 
     # ------------------------------------------------------------------ checks
-    def _check_inputs(self, q, k, v, den, want_device):
+    def _check_inputs(self, q, k, v, den, want_device, layout="hnd"):
         for name, t in (("q_rot", q), ("k_rot", k), ("v", v)):
             if t.dtype != torch.bfloat16:
                 raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
         if den.dtype != torch.float32:
             raise TypeError(f"normalizer must be float32, got {den.dtype}")
         if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
-            raise ValueError("q_rot, k_rot, v must share one [1, H, N, D] shape")
-        B, H, N, D = q.shape
+            raise ValueError("q_rot, k_rot, v must share one 4-D shape")
+        if layout == "hnd":
+            B, H, N, D = q.shape
+        elif layout == "nhd":
+            B, N, H, D = q.shape
+        else:
+            raise ValueError(f"layout must be 'hnd' or 'nhd', got {layout!r}")
         if B != 1:
             raise ValueError(f"batch must be 1, got {B}")
         if H != self.heads or D != self.head_dim:
@@ -156,16 +163,26 @@ class LinAttn:
         return N
 
     # ------------------------------------------------------------------ calls
-    def forward(self, q_rot, k_rot, v, normalizer, out=None, mode="high", out_dtype=torch.float32, stream=None):
-        """Enqueue one layer call on device tensors; returns ``out`` ([1, H, N, D])."""
-        n = self._check_inputs(q_rot, k_rot, v, normalizer, self.device)
+    def forward(self, q_rot, k_rot, v, normalizer, out=None, mode="high", out_dtype=torch.float32, stream=None,
+                layout="hnd"):
+        """Enqueue one layer call on device tensors and return ``out``.
+
+        layout "hnd": q_rot, k_rot, v and out are [1, H, N, D].
+        layout "nhd": q_rot, k_rot, v are [1, N, H, D] (the model's projection layout) and
+        out is [1, N, H*D] (any contiguous tensor of that many elements is accepted).
+        normalizer is [1, H, N, 1] either way."""
+        n = self._check_inputs(q_rot, k_rot, v, normalizer, self.device, layout)
         if out is None:
-            out = torch.empty(q_rot.shape, dtype=out_dtype, device=self.device)
-        elif out.shape != q_rot.shape or not out.is_contiguous() or out.device != self.device:
-            raise ValueError("out must be a contiguous [1, H, N, D] tensor on the context's device")
-        st = lib.lin_attn_forward(self._h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(),
-                                  out.data_ptr(), _out_code(out.dtype), n, _mode(mode),
-                                  _stream_handle(stream, self.device))
+            shape = q_rot.shape if layout == "hnd" else (1, n, self.heads * self.head_dim)
+            out = torch.empty(shape, dtype=out_dtype, device=self.device)
+        elif out.numel() != q_rot.numel() or not out.is_contiguous() or out.device != self.device:
+            raise ValueError("out must be a contiguous tensor of the inputs' size on the context's device")
+        args = (self._h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(), out.data_ptr(),
+                _out_code(out.dtype), n, _mode(mode))
+        if layout == "hnd":
+            st = lib.lin_attn_forward(*args, _stream_handle(stream, self.device))
+        else:
+            st = lib.lin_attn_forward_layout(*args, LAYOUT_NHD, _stream_handle(stream, self.device))
         _check(st, "lin_attn_forward")
         return out
 
