@@ -64,6 +64,10 @@ def _bind(lib):
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_bf16_decode.argtypes = [i64, p, p]
     lib.oracle_bf16_decode.restype = None
+    lib.oracle_f32_to_bf16.argtypes = [i64, p, p]
+    lib.oracle_f32_to_bf16.restype = None
+    lib.oracle_producer.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_double, p, p, p]
+    lib.oracle_producer.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -110,6 +114,31 @@ def bf16_decode(bits, lib=None) -> np.ndarray:
     return out
 
 
+def f32_to_bf16(values, lib=None) -> np.ndarray:
+    """binary32 -> BF16 bit patterns, round to nearest, ties to even."""
+    values = _f32(values)
+    out = np.empty(values.shape, np.uint16)
+    (lib or load()).oracle_f32_to_bf16(values.size, _ptr(values), _ptr(out))
+    return out
+
+
+def producer(q_bits, k_bits, cos, sin, eps=1e-6, lib=None):
+    """ReLU + interleaved RoPE + normaliser: (q_rot bits, k_rot bits, den FP64 [H, N])."""
+    q_bits, k_bits = _u16(q_bits), _u16(k_bits)
+    H, N, D = _shape3(q_bits)
+    if k_bits.shape != (H, N, D):
+        raise ValueError("q and k shapes differ")
+    cos, sin = _f32(cos).reshape(N, D // 2), _f32(sin).reshape(N, D // 2)
+    q_rot = np.empty((H, N, D), np.uint16)
+    k_rot = np.empty((H, N, D), np.uint16)
+    den = np.empty((H, N), np.float64)
+    rc = (lib or load()).oracle_producer(H, N, D, _ptr(q_bits), _ptr(k_bits), _ptr(cos), _ptr(sin), float(eps),
+                                         _ptr(q_rot), _ptr(k_rot), _ptr(den))
+    if rc:
+        raise RuntimeError(f"oracle_producer failed ({rc})")
+    return q_rot, k_rot, den
+
+
 def kv(k_bits, v_bits, lib=None) -> np.ndarray:
     """KV[h] = K[h]^T V[h] in FP64: [H, D, D]."""
     k_bits, v_bits = _u16(k_bits), _u16(v_bits)
@@ -124,11 +153,15 @@ def kv(k_bits, v_bits, lib=None) -> np.ndarray:
 
 
 def apply_rows(q_bits, kv_f64, den, rows=None, lib=None) -> np.ndarray:
-    """Normalised second GEMM for the given flat rows (h*N + n); [len(rows), D]."""
+    """Normalised second GEMM for the given flat rows (h*N + n); [len(rows), D].
+    den: FP32 denominators (the layer's input) or FP64 ones (from `producer`)."""
     q_bits = _u16(q_bits)
     H, N, D = _shape3(q_bits)
     kv_f64 = np.ascontiguousarray(kv_f64, dtype=np.float64)
-    den = _f32(den).reshape(H, N)
+    den = np.ascontiguousarray(den).reshape(H, N)
+    if den.dtype == np.float64:
+        return _apply_rows_f64den(q_bits, kv_f64, den, rows, lib)
+    den = _f32(den)
     if kv_f64.shape != (H, D, D):
         raise ValueError("kv shape mismatch")
     if rows is None:
@@ -142,6 +175,17 @@ def apply_rows(q_bits, kv_f64, den, rows=None, lib=None) -> np.ndarray:
     if rc:
         raise RuntimeError(f"oracle_apply_rows failed ({rc})")
     return out
+
+
+def _apply_rows_f64den(q_bits, kv_f64, den64, rows, lib):
+    # Same loops as oracle_apply_rows with the division by an FP64 denominator: run the
+    # FP32-denominator routine with den = 1 and divide here (both exact in FP64 up to the
+    # one rounding of each quotient).
+    H, N, D = q_bits.shape
+    ones = np.ones((H, N), np.float32)
+    num = apply_rows(q_bits, kv_f64, ones, rows, lib)
+    flat = np.arange(H * N) if rows is None else np.asarray(rows, np.int64)
+    return num / den64.reshape(-1)[flat][:, None]
 
 
 def forward(q_bits, k_bits, v_bits, den, lib=None) -> np.ndarray:

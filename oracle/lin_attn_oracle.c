@@ -20,6 +20,17 @@
  * Both quality tiers ('high', 'lossless') have this same exact target: they differ
  * only in rounding, so the oracle has no mode.
  *
+ * The producer step (oracle_producer) restates what the model does before the two GEMMs
+ * (page 1, snippet `sana_video.py`): ReLU on the normalised Q and K, interleaved RoPE on
+ * the activated copies (only the rotated copies feed the GEMMs), and the normaliser from
+ * the un-rotated activated copies:
+ *       qa = relu(q), ka = relu(k)
+ *       (y0, y1) of pair p of token n = (x0 c - x1 s, x0 s + x1 c), c = cos[n][p], s = sin[n][p]
+ *       den[h][n] = sum_i qa[h][n][i] * (sum_m ka[h][m][i]) + eps
+ * The rotation is fixed to IEEE binary32 operations in this order (each product and the
+ * sum rounded to nearest), then rounded once to BF16 (nearest, ties to even), so that any
+ * implementation following the same definition gets the same BF16 operands bit for bit.
+ *
  * Arithmetic: every input value (BF16 bit patterns, FP32 denominators) is exact
  * in FP64; products and sums are FP64 in the order written (m ascending for KV,
  * i ascending for the apply).  Build with -ffp-contract=off and no fast-math so
@@ -60,6 +71,75 @@ void oracle_set_num_threads(int n)
 #else
     (void)n;
 #endif
+}
+
+/* IEEE binary32 -> BF16, round to nearest, ties to even (NaN stays a quiet NaN). */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Round an array of binary32 values to BF16 bit patterns (tests pin the rounding). */
+void oracle_f32_to_bf16(int64_t count, const float *in, uint16_t *out)
+{
+    for (int64_t e = 0; e < count; ++e)
+        out[e] = f32_to_bf16_rne(in[e]);
+}
+
+/*
+ * Producer step: q, k are the BF16 bits of the normalised projections [H][N][D] (before
+ * ReLU), cos_t / sin_t the FP32 rotation tables [N][D/2].  Writes the BF16 bits of the
+ * rotated activated copies q_rot, k_rot [H][N][D] and the FP64 denominators den [H][N].
+ */
+int oracle_producer(int64_t H, int64_t N, int64_t D, const uint16_t *q, const uint16_t *k, const float *cos_t,
+                    const float *sin_t, double eps, uint16_t *q_rot, uint16_t *k_rot, double *den)
+{
+    if (H < 0 || N < 0 || D < 2 || D % 2 || !q || !k || !cos_t || !sin_t || !q_rot || !k_rot || !den)
+        return 1;
+    const int64_t P = D / 2;
+    int64_t h;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (h = 0; h < H; ++h) {
+        double *ksum = (double *)calloc((size_t)D, sizeof(double));
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t row = (h * N + n) * D;
+            for (int64_t i = 0; i < D; ++i) {
+                const double ka = bf16_to_f64(k[row + i]);
+                ksum[i] += ka > 0.0 ? ka : 0.0;
+            }
+        }
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t row = (h * N + n) * D;
+            double dot = 0.0;
+            for (int64_t i = 0; i < D; ++i) {
+                const double qa = bf16_to_f64(q[row + i]);
+                dot += (qa > 0.0 ? qa : 0.0) * ksum[i];
+            }
+            den[h * N + n] = dot + eps;
+            for (int64_t p = 0; p < P; ++p) {
+                const float c = cos_t[n * P + p], s = sin_t[n * P + p];
+                for (int which = 0; which < 2; ++which) {
+                    const uint16_t *src = which ? k : q;
+                    uint16_t *dst = which ? k_rot : q_rot;
+                    float x0 = (float)bf16_to_f64(src[row + 2 * p]);
+                    float x1 = (float)bf16_to_f64(src[row + 2 * p + 1]);
+                    x0 = x0 > 0.0f ? x0 : 0.0f;
+                    x1 = x1 > 0.0f ? x1 : 0.0f;
+                    const float a0 = x0 * c, b0 = x1 * s;
+                    const float a1 = x0 * s, b1 = x1 * c;
+                    dst[row + 2 * p] = f32_to_bf16_rne(a0 - b0);
+                    dst[row + 2 * p + 1] = f32_to_bf16_rne(a1 + b1);
+                }
+            }
+        }
+        free(ksum);
+    }
+    return 0;
 }
 
 /* Decode an array of BF16 bit patterns (used by tests to pin the decoding). */

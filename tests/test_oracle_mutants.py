@@ -25,6 +25,19 @@ MUTANTS = {
     "last_dim_dropped": ("for (int64_t i = 0; i < D; ++i)\n                s +=", "for (int64_t i = 0; i < D - 1; ++i)\n                s +="),
     "den_of_wrong_head": ("const double d = (double)den[flat];", "const double d = (double)den[flat % N];"),
 }
+# Slips in the producer step (ReLU, RoPE, normaliser, BF16 rounding).
+PRODUCER_MUTANTS = {
+    "rope_sign": ("dst[row + 2 * p] = f32_to_bf16_rne(a0 - b0);", "dst[row + 2 * p] = f32_to_bf16_rne(a0 + b0);"),
+    "rope_swapped_tables": ("const float c = cos_t[n * P + p], s = sin_t[n * P + p];",
+                            "const float s = cos_t[n * P + p], c = sin_t[n * P + p];"),
+    "rope_pair_shift": ("const float c = cos_t[n * P + p], s = sin_t[n * P + p];",
+                        "const float c = cos_t[n * P + (p + 1) % P], s = sin_t[n * P + (p + 1) % P];"),
+    "no_relu_on_rotated": ("x0 = x0 > 0.0f ? x0 : 0.0f;", "x0 = x0;"),
+    "no_relu_in_den": ("ksum[i] += ka > 0.0 ? ka : 0.0;", "ksum[i] += ka;"),
+    "rounding_truncates": ("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0u;"),
+    "rounding_ties_away": ("u += 0x7fffu + ((u >> 16) & 1u);", "u += 0x8000u;"),
+    "eps_dropped": ("den[h * N + n] = dot + eps;", "den[h * N + n] = dot;"),
+}
 
 
 def pins_hold(lib) -> bool:
@@ -43,8 +56,33 @@ def pins_hold(lib) -> bool:
     return True
 
 
+def producer_pins_hold(lib) -> bool:
+    from test_oracle_producer_pins import random_case, torch_producer
+    for shape in ((2, 64, 32), (3, 17, 112)):
+        q, k, cos, sin = random_case(*shape, seed=sum(shape))
+        q_rot, k_rot, den = oracle.producer(q, k, cos, sin, lib=lib)
+        tq, tk, tden = torch_producer(q, k, cos, sin)
+        if not (np.array_equal(q_rot, tq) and np.array_equal(k_rot, tk) and np.allclose(den, tden, rtol=1e-13)):
+            return False
+    vals = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 1.2345678], np.float32)
+    import torch
+    from conftest import bf16_bits
+    return bool(np.array_equal(oracle.f32_to_bf16(vals, lib=lib), bf16_bits(torch.from_numpy(vals).to(torch.bfloat16))))
+
+
 def test_unmodified_oracle_passes(oracle_lib):
     assert pins_hold(oracle_lib)
+    assert producer_pins_hold(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(PRODUCER_MUTANTS))
+def test_producer_mutant_is_caught(tmp_path, name):
+    old, new = PRODUCER_MUTANTS[name]
+    assert SRC.count(old) >= 1, f"mutation site for {name} not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(SRC.replace(old, new))
+    lib = oracle.load(lib_path=str(tmp_path / f"lib{name}.so"), src=str(src))
+    assert not producer_pins_hold(lib), f"pins missed the planted slip {name}"
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -25,7 +25,9 @@ Recipe (draw order is fixed; one ``torch.Generator`` seeded with ``seed``):
   4. ``den[h, n] = q_pre[h, n, :] . sum_m k_pre[h, m, :] + 1e-6`` in FP64,
      rounded once to FP32 (a denominator: the layer divides by it).
 
-All tensors are contiguous ``[1, H, N, D]`` (``den``: ``[1, H, N, 1]``).
+All tensors are contiguous ``[1, H, N, D]`` (``den``: ``[1, H, N, 1]``).  On request the
+generator also returns the pre-ReLU ``q``, ``k`` and the FP32 rotation tables, the inputs
+of the fused producer path.
 """
 from __future__ import annotations
 
@@ -109,30 +111,39 @@ def _rotate_pairs(x: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor) -> torc
     return out
 
 
-def make_layer(heads: int, tokens: int, head_dim: int, seed: int = 0, grid=None, device="cpu"):
-    """One layer's inputs: dict of q_rot, k_rot, v (BF16) and den (FP32)."""
+def make_layer(heads: int, tokens: int, head_dim: int, seed: int = 0, grid=None, device="cpu",
+               producer_inputs: bool = False):
+    """One layer's inputs: dict of q_rot, k_rot, v (BF16) and den (FP32).
+
+    With producer_inputs, also the tensors the layer starts from before ReLU, RoPE and the
+    normaliser: "q", "k" (BF16 [1, H, N, D], the normalised projections before ReLU) and
+    the rotation tables "rope_cos", "rope_sin" (FP32 [N, D/2])."""
     if head_dim % 2:
         raise ValueError("head_dim must be even for pairwise RoPE")
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     shape = (heads, tokens, head_dim)
-    q_pre = torch.relu(torch.randn(shape, generator=g, device=device)).to(torch.bfloat16)
-    k_pre = torch.relu(torch.randn(shape, generator=g, device=device)).to(torch.bfloat16)
+    q_in = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    k_in = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    q_pre, k_pre = torch.relu(q_in), torch.relu(k_in)
     v = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
     cos, sin = rope_tables(tokens, head_dim, grid, device)
     q_rot = _rotate_pairs(q_pre.float(), cos, sin).to(torch.bfloat16)
     k_rot = _rotate_pairs(k_pre.float(), cos, sin).to(torch.bfloat16)
-    del cos, sin
     ksum = k_pre.double().sum(dim=1)  # [H, D]
     den = (torch.einsum("hnd,hd->hn", q_pre.double(), ksum) + EPS).to(torch.float32)
     del q_pre, k_pre, ksum
-    return {
+    out = {
         "q_rot": q_rot.unsqueeze(0).contiguous(),
         "k_rot": k_rot.unsqueeze(0).contiguous(),
         "v": v.unsqueeze(0).contiguous(),
         "den": den.reshape(1, heads, tokens, 1).contiguous(),
     }
+    if producer_inputs:
+        out.update(q=q_in.unsqueeze(0).contiguous(), k=k_in.unsqueeze(0).contiguous(),
+                   rope_cos=cos.contiguous(), rope_sin=sin.contiguous())
+    return out
 
 
-def make_workload(w: Workload, device="cpu"):
-    return make_layer(w.heads, w.tokens, w.head_dim, w.seed, w.grid, device)
+def make_workload(w: Workload, device="cpu", producer_inputs: bool = False):
+    return make_layer(w.heads, w.tokens, w.head_dim, w.seed, w.grid, device, producer_inputs)
