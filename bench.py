@@ -242,7 +242,8 @@ def run_ours(args, w, world, rank, local, dist):
     out_bytes = 4 if out_dtype == torch.float32 else 2
     # --layers L: L distinct layers with their own seeded inputs (a denoise step's worth),
     # visited in turn, one per step.
-    layers = [synth.make_layer(H, N, D, w.seed + rank * args.layers + i, w.grid, device=dev)
+    layers = [synth.make_layer(H, N, D, w.seed + rank * args.layers + i, w.grid, device=dev,
+                               producer_inputs=args.fused)
               for i in range(args.layers)]
     if args.layout == "nhd":  # the model's [1, N, H, D] projection layout
         for g in layers:
@@ -257,8 +258,11 @@ def run_ours(args, w, world, rank, local, dist):
     def step():
         g = layers[counter[0] % len(layers)]
         counter[0] += 1
-        ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream,
-                    layout=args.layout)
+        if args.fused:
+            ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out=out, stream=stream)
+        else:
+            ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream,
+                        layout=args.layout)
 
     for _ in range(args.warmup):
         step()
@@ -313,6 +317,10 @@ def run_ours(args, w, world, rank, local, dist):
     d2h = H * N * D * out_bytes
 
     nbytes = algorithmic_bytes(H, N, D, out_bytes)
+    if args.fused:  # no denominator input; the FP32 rotation tables are read once
+        tables = 2 * N * (D // 2) * 4
+        nbytes = {"kv_partial": nbytes["kv_partial"] + tables, "apply": nbytes["apply"] - H * N * 4,
+                  "total": nbytes["total"] - H * N * 4 + tables}
     peak, peak_kind = load_peaks()
     dom = max(("kv_partial", "apply"), key=lambda k: stage_ms[k])
     achieved = nbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
@@ -332,6 +340,7 @@ def run_ours(args, w, world, rank, local, dist):
                 "l2": "inputs larger than L2; consecutive steps use different layers' inputs (no flush needed)",
                 "bytes_per_call": nbytes["total"], "parallelism": f"replicas x{world}",
                 "layers": args.layers, "layout": args.layout,
+                "producer": "fused (ReLU + RoPE + normaliser in the kernels)" if args.fused else "inputs pre-rotated",
             },
             "achieved_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
             "stage_ms": stage_ms,
@@ -364,6 +373,8 @@ def main():
                     help="distinct seeded layers visited in turn, one per step (2: no step finds the previous "
                          "step's data in L2)")
     ap.add_argument("--layout", default="hnd", choices=["hnd", "nhd"], help="activation layout of the timed calls")
+    ap.add_argument("--fused", action="store_true",
+                    help="time lin_attn_forward_fused (pre-activation q, k and rotation tables in)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()

@@ -111,6 +111,27 @@ int lin_attn_forward_layout(lin_attn_ctx *ctx, const void *q_rot, const void *k_
                             int mode, int layout, struct CUstream_st *stream);
 
 /*
+ * The layer call with the producer step fused in ('high' tier): what the model does right
+ * before the two GEMMs (page 1, 关键源码片段, `sana_video.py`: `F.relu` on the normalised
+ * query and key, `apply_interleaved_rotary_emb` on the activated copies, and the normaliser
+ * from the un-rotated activated copies) runs inside the kernels, on the tiles they load.
+ *   q, k     : BF16 [1, H, N, D], the normalised projections BEFORE ReLU and RoPE
+ *   v        : BF16 [1, H, N, D]
+ *   rope_cos, rope_sin : FP32 [N, D/2]; pair p (elements 2p, 2p+1) of token n turns by
+ *              (rope_cos, rope_sin)[n][p]
+ *   out      : as lin_attn_forward (head-major)
+ * Computes qa = relu(q), ka = relu(k); Q_rot, K_rot = each pair (x0, x1) of qa, ka turned to
+ * (x0 c - x1 s, x0 s + x1 c) with binary32 products and sums in exactly that order, rounded
+ * once to BF16 (nearest-even); den[h][n] = qa[h][n] . (sum over m of ka[h][m]) + 1e-6; then
+ * the two GEMMs and the normalisation of lin_attn_forward.  The column sums of relu(K) are
+ * accumulated in FP64 and reduced in a fixed order.  mode must be LIN_ATTN_MODE_HIGH
+ * (LIN_ATTN_ERR_UNSUPPORTED otherwise).
+ */
+int lin_attn_forward_fused(lin_attn_ctx *ctx, const void *q, const void *k, const void *v,
+                           const float *rope_cos, const float *rope_sin, void *out, int out_dtype,
+                           int64_t n_tokens, int mode, struct CUstream_st *stream);
+
+/*
  * Same layer call on HOST buffers (same shapes and dtypes, any alignment).  Copies the
  * inputs to device staging owned by the context, runs the layer, copies the result
  * back and synchronises `stream` before returning: when it returns OK, `out` holds the

@@ -1,0 +1,103 @@
+"""The fused producer path (lin_attn_forward_fused): ReLU, interleaved RoPE and the
+normaliser computed inside the kernels from the pre-activation q, k and FP32 rotation
+tables.  Held to the FP64 oracle (its producer step, then the layer) with the same
+tolerances as the plain call; and because the rotation is defined bit for bit, the reduced
+KV must equal, bitwise, the KV the plain call forms from the generator's Q_rot/K_rot."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import bf16_bits, rel_l2
+from video_diffusion_dit_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 2e-5, torch.bfloat16: 4e-3}
+
+
+@pytest.fixture(scope="module")
+def la():
+    from video_diffusion_dit_gb300 import lin_attn
+    return lin_attn
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = torch.device("cuda", 0)
+    torch.cuda.set_device(d)
+    return d
+
+
+def oracle_fused(layer, rows=None):
+    """Producer step then the layer, all on the oracle; rows = flat sample or None (all)."""
+    q, k = bf16_bits(layer["q"][0]), bf16_bits(layer["k"][0])
+    q_rot, k_rot, den = oracle.producer(q, k, layer["rope_cos"].cpu().numpy(), layer["rope_sin"].cpu().numpy())
+    kv = oracle.kv(k_rot, bf16_bits(layer["v"][0]))
+    out = oracle.apply_rows(q_rot, kv, den, rows)
+    return out, kv
+
+
+def check(la, dev, H, N, D, seed, grid=None, dtypes=(torch.float32, torch.bfloat16)):
+    layer = synth.make_layer(H, N, D, seed, grid, producer_inputs=True)
+    ref, kv_ref = oracle_fused(layer)
+    ref = ref.reshape(H, N, D)
+    g = {key: t.to(dev) for key, t in layer.items()}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for dt in dtypes:
+            out = ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out_dtype=dt)
+            assert ctx.device_status() == 0
+            err = rel_l2(out.double().cpu().numpy()[0], ref)
+            assert err <= TOL[dt], f"fused H={H} N={N} D={D} {dt}: rel-L2 {err:.3e}"
+        kv_fused = ctx.debug_kv().clone()
+        assert rel_l2(kv_fused.double().cpu().numpy(), kv_ref) <= 1e-6
+        # The plain call on the generator's rotated operands forms bitwise the same KV.
+        plain = ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"])
+        assert torch.equal(ctx.debug_kv(), kv_fused)
+        fused = ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"])
+        # Only the denominators differ (FP32 in the kernel vs FP64 -> FP32 in the generator).
+        assert rel_l2(fused.double().cpu().numpy(), plain.double().cpu().numpy()) <= 1e-6
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 32), (3, 777, 112), (2, 1000, 64), (4, 129, 128), (1, 1, 16),
+                                   (2, 65, 48)])
+def test_fused_small(la, dev, shape):
+    check(la, dev, *shape, seed=shape[1])
+
+
+def test_fused_480p(la, dev):
+    w = synth.WORKLOADS["480p_81f"]
+    check(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid, dtypes=(torch.float32,))
+
+
+def test_fused_720p_sampled(la, dev):
+    w = synth.WORKLOADS["720p_193f"]
+    H, N, D = w.heads, w.tokens, w.head_dim
+    layer = synth.make_workload(w, device=dev, producer_inputs=True)
+    rows = np.unique(np.concatenate([np.random.default_rng(2).choice(H * N, 2048, replace=False),
+                                     [0, N - 1, N, H * N - 1]])).astype(np.int64)
+    ref, kv_ref = oracle_fused(layer, rows)
+    with la.LinAttn(H, N, D, dev) as ctx:
+        out = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"])
+        assert ctx.device_status() == 0
+        got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        assert rel_l2(got, ref) <= TOL[torch.float32]
+        assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= 1e-6
+        again = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"]).clone()
+        third = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"])
+        assert torch.equal(again, third)
+
+
+def test_fused_rejects_lossless_and_bad_tables(la, dev):
+    g = {k: t.to(dev) for k, t in synth.make_layer(2, 64, 32, 0, producer_inputs=True).items()}
+    with la.LinAttn(2, 64, 32, dev) as ctx:
+        out = torch.empty(1, 2, 64, 32, device=dev)
+        s = torch.cuda.current_stream().cuda_stream
+        args = [g["q"].data_ptr(), g["k"].data_ptr(), g["v"].data_ptr(), g["rope_cos"].data_ptr(),
+                g["rope_sin"].data_ptr(), out.data_ptr(), la.OUT_F32, 64]
+        assert la.lib.lin_attn_forward_fused(ctx._h, *args, la.MODE_LOSSLESS, s) == la.ERR_UNSUPPORTED
+        bad = list(args)
+        bad[3] = 0
+        assert la.lib.lin_attn_forward_fused(ctx._h, *bad, la.MODE_HIGH, s) == la.ERR_INVALID_ARG
+        with pytest.raises(ValueError):
+            ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"][:32], g["rope_sin"])

@@ -26,20 +26,22 @@ namespace {
 // KV, so the result has FP32-class accuracy (the tier's second GEMM "stays FP32").
 constexpr int kApplyStages = 3;
 constexpr int kApplyThreads = 192;
+constexpr int kApplyThreadsFused = 448;  // + warps 6..13: the producer-step transform
+constexpr int kApplyTransformThreads = 256;
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
 constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
 
-__host__ __device__ inline uint32_t apply_smem_bytes(int head_dim) {
+__host__ __device__ inline uint32_t apply_smem_bytes(int head_dim, bool fused) {
     const uint32_t nbox = head_dim_atoms(head_dim);
     return static_cast<uint32_t>(kv_image_bytes(head_dim)) + kApplyStages * nbox * kQAtomBytes +
-           4 * 2 * kOutBoxBytes + 256 + 1024;
+           4 * 2 * kOutBoxBytes + 256 + (fused ? 2 * kApplyTile * 4 : 0) + 1024;
 }
 
-template <int NBOX, bool OUT_BF16>
-__global__ void __launch_bounds__(kApplyThreads, 1)
+template <int NBOX, bool OUT_BF16, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                     const uint8_t* __restrict__ kv_image, const float* __restrict__ den, int heads, int n_tokens,
-                    int head_dim, int tiles_per_head, int token_major, int* status) {
+                    int head_dim, int tiles_per_head, int token_major, int* status, const ProducerArgs pa) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -59,8 +61,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
     const uint32_t b_full = acc_empty0 + 16u;
     const uint32_t b_empty = b_full + 8u;
     const uint32_t drain_bar = b_empty + 8u;
+    const uint32_t q_ready0 = drain_bar + 8u;             // [kApplyStages] (fused: tile transformed)
+    const uint32_t den_full0 = q_ready0 + 8u * kApplyStages;  // [2] (fused: row denominators written)
+    const uint32_t den_empty0 = den_full0 + 16u;          // [2] (fused: row denominators read)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + 200);
+    float* den_s = reinterpret_cast<float*>(base_ptr + bar_off + 256);  // fused: [2][kApplyTile]
+    const uint32_t mma_ready0 = FUSED ? q_ready0 : q_full0;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -72,8 +79,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         for (int s = 0; s < kApplyStages; ++s) {
             mbar_init(q_full0 + 8u * s, 1);
             mbar_init(q_empty0 + 8u * s, 1);
+            if (FUSED) mbar_init(q_ready0 + 8u * s, kApplyTransformThreads);
         }
         for (int b = 0; b < 2; ++b) {
+            if (FUSED) {
+                mbar_init(den_full0 + 8u * b, kApplyTransformThreads);
+                mbar_init(den_empty0 + 8u * b, 4);
+            }
             mbar_init(acc_full0 + 8u * b, 1);
             mbar_init(acc_empty0 + 8u * b, 4);
         }
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                 if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
-                if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
+                if (!mbar_wait(mma_ready0 + 8u * st, ph, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 128u;
                 const uint32_t qa = q_smem + st * NBOX * kQAtomBytes;
@@ -188,7 +200,73 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             mma_commit(drain_bar);
             mbar_wait_drain(drain_bar, 0);
         }
-    } else {
+    } else if (FUSED && warp >= 6) {
+        // ---------------- producer-step transform of the Q tiles (fused path)
+        // Thread (chunk c, row group rg) takes columns 8c..8c+7 of rows rg, rg+16, ..., rg+112:
+        // ReLU, dot with the head's column sums of relu(K) (the normaliser), then the rotation
+        // (binary32 products and sum in a fixed order, rounded once to BF16).  The 16 threads of
+        // a row add their dot products in a fixed butterfly; the row's denominator goes to
+        // den_s for the epilogue.  The tile's table rows are requested before its wait.
+        const int u = threadIdx.x - 192;
+        const int c = u & 15, rg = u >> 4;
+        const bool live = 8 * c < head_dim;
+        const int64_t pairs = head_dim / 2;
+        const uint64_t tpol = policy_evict_last();
+        float ks[8];
+        int cur_h = -1;
+        uint32_t it = 0;
+        for (int t = t_begin; t < t_end; ++t, ++it) {
+            const int h = t / tiles_per_head;
+            const int n0 = (t % tiles_per_head) * kApplyTile;
+            const uint32_t lt = static_cast<uint32_t>(t - t_begin);
+            float4 cv[8], sv[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int n = n0 + rg + 16 * k;
+                if (live && n < n_tokens) {
+                    cv[k] = ldg_f4_hint(pa.cos + n * pairs + 4 * c, tpol);
+                    sv[k] = ldg_f4_hint(pa.sin + n * pairs + 4 * c, tpol);
+                } else {
+                    cv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    sv[k] = cv[k];
+                }
+            }
+            if (h != cur_h) {
+                if (cur_h < 0) grid_dependency_wait();  // the column sums come from the reduction
+                cur_h = h;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ks[e] = live ? pa.ksum[h * head_dim + 8 * c + e] : 0.f;
+            }
+            const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
+            const uint32_t buf = lt & 1u;
+            if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
+            if (!mbar_wait(den_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+            uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kQAtomBytes;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = rg + 16 * k;
+                const int n = n0 + r;
+                float part = 0.f;
+                if (live && n < n_tokens) {
+                    uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                    uint4 w = *cell;
+                    float act[8];
+                    rope_chunk(w, cv[k], sv[k], act);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part = __fmaf_rn(act[e], ks[e], part);
+                    *cell = w;
+                }
+                part += __shfl_xor_sync(0xffffffffu, part, 8);
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                if (c == 0) den_s[buf * kApplyTile + r] = part + kDenEps;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(q_ready0 + 8u * st);
+            mbar_arrive(den_full0 + 8u * buf);
+        }
+    } else if (!FUSED || warp < 6) {
         // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes / tile rows 32q..32q+31
         const int q = warp & 3;
         const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
@@ -202,9 +280,17 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
             const int row0 = n0 + 32 * q;
             const int row = row0 + lane;
-            const float dv = row < n_tokens ? den[static_cast<int64_t>(h) * n_tokens + row] : 1.0f;
-            const float rcp = __frcp_rn(dv);
             const uint32_t buf = lt & 1u;
+            float dv = 1.0f;
+            if (FUSED) {
+                if (!mbar_wait(den_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status)) break;
+                dv = den_s[buf * kApplyTile + 32 * q + lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(den_empty0 + 8u * buf);
+            } else if (row < n_tokens) {
+                dv = den[static_cast<int64_t>(h) * n_tokens + row];
+            }
+            const float rcp = __frcp_rn(dv);
             if (!mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
@@ -362,17 +448,30 @@ __global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restr
     }
 }
 
-template <int NBOX, bool BF16>
+template <int NBOX, bool BF16, bool FUSED>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
                       int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
-                      cudaStream_t stream) {
-    const uint32_t smem = apply_smem_bytes(head_dim);
-    cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                      cudaStream_t stream, const ProducerArgs& pa) {
+    const uint32_t smem = apply_smem_bytes(head_dim, FUSED);
+    cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
-    return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
-                             img, den, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status);
+    return launch_overlapped(apply_tc_kernel<NBOX, BF16, FUSED>, dim3(grid),
+                             dim3(FUSED ? kApplyThreadsFused : kApplyThreads), smem, stream, tm_q, tm_out, img, den,
+                             heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, pa);
+}
+
+template <int NBOX, bool BF16>
+cudaError_t launch_tc_any(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
+                          int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
+                          cudaStream_t stream, const ProducerArgs* producer) {
+    if (producer)
+        return launch_tc<NBOX, BF16, true>(tm_q, tm_out, img, den, heads, n_tokens, head_dim, token_major, grid,
+                                           status, stream, *producer);
+    const ProducerArgs none{nullptr, nullptr, nullptr, nullptr, 0};
+    return launch_tc<NBOX, BF16, false>(tm_q, tm_out, img, den, heads, n_tokens, head_dim, token_major, grid, status,
+                                        stream, none);
 }
 
 template <int C, bool BF16>
@@ -409,16 +508,17 @@ cudaError_t dispatch_ffma(const uint16_t* q, Strides sd, const float* kv, const 
 
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, cudaStream_t stream) {
+                            bool token_major, int grid, int* status, cudaStream_t stream,
+                            const ProducerArgs* producer) {
     const int n = static_cast<int>(n_tokens);
     const int total = heads * ((n + kApplyTile - 1) / kApplyTile);
     if (grid > total) grid = total;
     const bool one = head_dim_atoms(head_dim) == 1;
     if (one)
-        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
-                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
-    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
-                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
+        return out_bf16 ? launch_tc_any<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer)
+                        : launch_tc_any<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer);
+    return out_bf16 ? launch_tc_any<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer)
+                    : launch_tc_any<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer);
 }
 
 cudaError_t launch_apply_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,

@@ -25,15 +25,20 @@ namespace {
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
+constexpr int kKvThreadsFused = 320;  // + warps 6..9: the producer-step transform
 constexpr int kKvPromoteTiles = 4;  // tiles per tensor-core sub-chunk (256 tokens)
 constexpr uint32_t kKvAtomBytes = kKvTile * 128;  // one box: 64 token rows x 128 bytes
 
-template <int NBOX>
+template <int NBOX, bool FUSED>
 struct KvLayout {
+    // The fused path also stages the tile's rows of the two rotation tables (FP32,
+    // [64 tokens][D/2], at most 16 KB each), so it runs with fewer, larger stages.
+    static constexpr int stages = FUSED ? 3 : kKvStages;
     static constexpr uint32_t a_bytes = 2 * kKvAtomBytes;  // A = K^T: 2 atoms cover M = 128
     static constexpr uint32_t b_bytes = NBOX * kKvAtomBytes;
-    static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
-    static constexpr uint32_t bar_offset = kKvStages * stage_bytes;
+    static constexpr uint32_t tab_bytes = kKvTile * 64 * 4;  // one table's rows, D/2 <= 64 columns
+    static constexpr uint32_t stage_bytes = a_bytes + b_bytes + (FUSED ? 2 * tab_bytes : 0);
+    static constexpr uint32_t bar_offset = stages * stage_bytes;
     static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;  // + barriers + alignment slack
 };
 
@@ -49,23 +54,25 @@ __device__ __forceinline__ ChunkTiles chunk_tiles(const KvPlan& plan, const KvLa
     return r;
 }
 
-template <int NBOX>
-__global__ void __launch_bounds__(kKvThreads, 1)
+template <int NBOX, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     kv_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          float* __restrict__ partial, int head_dim, const KvPlan plan, const KvLaunch work,
-                         int token_major, int* status) {
-    using L = KvLayout<NBOX>;
+                         int token_major, int* status, const ProducerArgs pa,
+                         const __grid_constant__ CUtensorMap tm_cos, const __grid_constant__ CUtensorMap tm_sin) {
+    using L = KvLayout<NBOX, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
 
     const uint32_t bars = base + L::bar_offset;
-    const uint32_t full0 = bars;                          // [kKvStages]
-    const uint32_t empty0 = bars + 8u * kKvStages;        // [kKvStages]
-    const uint32_t acc_full0 = bars + 16u * kKvStages;    // [2]
+    const uint32_t full0 = bars;                          // [L::stages]
+    const uint32_t empty0 = bars + 8u * L::stages;        // [L::stages]
+    const uint32_t acc_full0 = bars + 16u * L::stages;    // [2]
     const uint32_t acc_empty0 = acc_full0 + 16u;          // [2]
     const uint32_t drain_bar = acc_empty0 + 16u;
+    const uint32_t ready0 = drain_bar + 8u;               // [L::stages] (fused: tile transformed)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 200);
 
@@ -73,11 +80,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int lane = threadIdx.x & 31;
     const ChunkTiles ct = chunk_tiles(plan, work);
     const int64_t tph = plan.tiles_per_head;
+    // The MMA consumes a stage once it is loaded (full) or, on the fused path, transformed.
+    const uint32_t mma_ready0 = FUSED ? ready0 : full0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kKvStages; ++s) {
+        for (int s = 0; s < L::stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
+            if (FUSED) mbar_init(ready0 + 8u * s, 128);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
@@ -89,7 +99,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     }
     if (NBOX == 1) {
         // Head dim <= 64: the second A atom (rows i = 64..127) is never loaded; zero it once.
-        for (uint32_t idx = threadIdx.x; idx < kKvStages * (kKvAtomBytes / 16); idx += blockDim.x) {
+        for (uint32_t idx = threadIdx.x; idx < L::stages * (kKvAtomBytes / 16); idx += blockDim.x) {
             const uint32_t st = idx / (kKvAtomBytes / 16), off = idx % (kKvAtomBytes / 16);
             *reinterpret_cast<uint4*>(base_ptr + st * L::stage_bytes + kKvAtomBytes + off * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -103,6 +113,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        if (FUSED) {
+            prefetch_tmap(&tm_cos);
+            prefetch_tmap(&tm_sin);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -117,31 +131,39 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (lane == 0) {
             // ---------------- producer: every tile of the chunk, in order
             const uint64_t pol = policy_evict_first();
+            const uint64_t tab_pol = policy_evict_last();
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
                 const int h = static_cast<int>(t / tph);
                 const int y = static_cast<int>((t % tph) * kKvTile);
                 const int c1 = token_major ? h - work.h0 : y, c2 = token_major ? y : h - work.h0;
-                const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
+                const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
                 if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 const uint32_t a = base + st * L::stage_bytes;
                 const uint32_t b = a + L::a_bytes;
-                mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
+                const uint32_t tab_tx = FUSED ? 2u * kKvTile * (head_dim / 2) * 4u : 0u;
+                mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes + tab_tx);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x) {
                     tma_load_3d_hint(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, c1, c2, pol);
                     tma_load_3d_hint(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, c1, c2, pol);
                 }
+                if (FUSED) {
+                    // rotation-table rows of the tile's tokens (kept in L2: every head re-reads them)
+                    const uint32_t tab = b + L::b_bytes;
+                    tma_load_2d_hint(tab, &tm_cos, full0 + 8u * st, 0, y, tab_pol);
+                    tma_load_2d_hint(tab + L::tab_bytes, &tm_sin, full0 + 8u * st, 0, y, tab_pol);
+                }
             }
             if (!ok) {
                 // Let the loads already issued land before shared memory goes away.
-                const uint32_t first = it > kKvStages ? it - kKvStages : 0;
+                const uint32_t first = it > L::stages ? it - L::stages : 0;
                 for (uint32_t j = first; j < it; ++j)
-                    mbar_wait_drain(full0 + 8u * (j % kKvStages), (j / kKvStages) & 1u);
+                    mbar_wait_drain(full0 + 8u * (j % L::stages), (j / L::stages) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -166,8 +188,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     tc_fence_after();
                     const uint32_t d = tmem + buf * 128u;
                     for (int64_t k = k0; k < k1; ++k, ++it) {
-                        const uint32_t st = it % kKvStages, ph = (it / kKvStages) & 1u;
-                        if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status)) {
+                        const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
+                        if (!mbar_wait(mma_ready0 + 8u * st, ph, abort_flag, status)) {
                             ok = false;
                             break;
                         }
@@ -190,7 +212,68 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_commit(drain_bar);
             mbar_wait_drain(drain_bar, 0);
         }
-    } else {
+    } else if (FUSED && warp >= 6) {
+        // ---------------- producer-step transform of the K tiles (fused path)
+        const int u = threadIdx.x - 192;
+        const int c = u & 15, rg = u >> 4;
+        const bool live = 8 * c < head_dim;
+        const int64_t pairs = head_dim / 2;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
+            const int h = static_cast<int>(t / tph);
+            const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+            // Column sums of relu(K), compensated binary32 summation (sum + running error
+            // term, fixed order): FP64-class accuracy at FP32 rate.
+            float ks[8], kc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ks[e] = kc[e] = 0.f;
+            for (; t < seg_end; ++t, ++it) {
+                const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
+                if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                if (live) {
+                    const int n0 = static_cast<int>((t % tph) * kKvTile);
+                    uint8_t* stage = base_ptr + st * L::stage_bytes;
+                    uint8_t* atom = stage + (c >> 3) * kKvAtomBytes;
+                    const uint8_t* tab = stage + L::a_bytes + L::b_bytes + 16 * c;  // [64][pairs] floats
+#pragma unroll
+                    for (int k8 = 0; k8 < kKvTile / 8; ++k8) {
+                        const int r = rg + 8 * k8;
+                        if (n0 + r < pa.n_tokens) {  // rows past the end stay zero
+                            uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                            uint4 w = *cell;
+                            const float4 c4 = *reinterpret_cast<const float4*>(tab + r * pairs * 4);
+                            const float4 s4 = *reinterpret_cast<const float4*>(tab + L::tab_bytes + r * pairs * 4);
+                            float act[8];
+                            rope_chunk(w, c4, s4, act);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float yv = __fsub_rn(act[e], kc[e]);
+                                const float tsum = __fadd_rn(ks[e], yv);
+                                kc[e] = __fsub_rn(__fsub_rn(tsum, ks[e]), yv);
+                                ks[e] = tsum;
+                            }
+                            *cell = w;
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(ready0 + 8u * st);
+            }
+            if (!ok) break;
+            // This row group's column sums of the segment: [h][slot][rg][column] (the
+            // reduction adds the 8 row groups in order, then the segments).
+            if (live) {
+                const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
+                double* dst = pa.ksum_partial + (slot * 8 + rg) * head_dim + 8 * c;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[e] = static_cast<double>(ks[e]) - static_cast<double>(kc[e]);
+            }
+        }
+    } else if (!FUSED || warp < 6) {
         // ---------------- epilogue: TMEM lanes 32q..32q+31 = rows i of the partial KV.
         // Thread i keeps its row of the segment's running sum in registers.
         const int q = warp & 3;
@@ -385,9 +468,49 @@ __device__ __forceinline__ float reduce_segments(const float* p, int64_t stride,
 // adds the partials of one element (loads coalesced across the 32 columns), then the
 // tile goes through shared memory so that 32 threads each write one 16-byte chunk (8
 // consecutive rows i of column j) per term of the image.
+// Fixed-order sum of a head's FP64 column-sum partials (fused path): each segment's value
+// is its 8 row-group sums added in order (p[s][0..7], `stride` apart), then the segments
+// are added with the same tree as above.
+__device__ __forceinline__ double segment_value_f64(const double* p, int64_t stride, int s) {
+    const double* q = p + static_cast<int64_t>(s) * 8 * stride;
+    double v = q[0];
+#pragma unroll
+    for (int g = 1; g < 8; ++g) v += q[g * stride];
+    return v;
+}
+__device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t stride, int nseg) {
+    double groups[kTreeGroups];
+    int ngroups = 0;
+#pragma unroll
+    for (int g = 0; g < kTreeGroups; ++g) {
+        const int g0 = g * kTreeGroup;
+        groups[g] = 0.0;
+        if (g0 < nseg) {
+            double vals[kTreeGroup];
+#pragma unroll
+            for (int s = 0; s < kTreeGroup; ++s) vals[s] = g0 + s < nseg ? segment_value_f64(p, stride, g0 + s) : 0.0;
+#pragma unroll
+            for (int w = 1; w < kTreeGroup; w *= 2)
+#pragma unroll
+                for (int s = 0; s + w < kTreeGroup; s += 2 * w)
+                    if (s + w < nseg - g0) vals[s] = vals[s] + vals[s + w];
+            groups[g] = vals[0];
+            ngroups = g + 1;
+        }
+    }
+#pragma unroll
+    for (int w = 1; w < kTreeGroups; w *= 2)
+#pragma unroll
+        for (int s = 0; s + w < kTreeGroups; s += 2 * w)
+            if (s + w < ngroups) groups[s] = groups[s] + groups[s + w];
+    return groups[0];
+}
+
 __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restrict__ partial,
                                                           float* __restrict__ kv, uint8_t* __restrict__ image,
-                                                          int h0, int head_dim, const KvPlan plan) {
+                                                          int h0, int head_dim, const KvPlan plan,
+                                                          const double* __restrict__ ksum_partial,
+                                                          float* __restrict__ ksum) {
     grid_launch_dependents();  // the apply kernel may start its prologue and Q loads now
     grid_dependency_wait();    // the partials of this call are complete past this point
     __shared__ float tile[8][33];
@@ -398,6 +521,11 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
     const int e = threadIdx.x >> 5, jl = threadIdx.x & 31;
     const int i = 8 * r + e, j = j0 + jl;
     const int nseg = segments_of_head(plan, h);
+    if (ksum_partial != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < head_dim) {
+        // Fused path: column sums of relu(K) over all tokens, rounded once to FP32.
+        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * 8 * head_dim + threadIdx.x;
+        ksum[h * head_dim + threadIdx.x] = static_cast<float>(reduce_segments_f64(kp, head_dim, nseg));
+    }
     float x = 0.f;
     if (j < head_dim) {
         const float* p = partial + static_cast<int64_t>(h) * plan.seg_stride * dd + i * head_dim + j;
@@ -438,15 +566,17 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
     *reinterpret_cast<uint4*>(img + 2 * term_bytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-template <int NBOX>
+template <int NBOX, bool FUSED>
 cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int head_dim,
-                      const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, cudaStream_t stream) {
-    using L = KvLayout<NBOX>;
-    cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::smem_bytes);
+                      const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, cudaStream_t stream,
+                      const ProducerArgs& pa, const CUtensorMap& tm_cos, const CUtensorMap& tm_sin) {
+    using L = KvLayout<NBOX, FUSED>;
+    cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_overlapped(kv_partial_tc_kernel<NBOX>, dim3(work.n_chunks), dim3(kKvThreads), L::smem_bytes, stream,
-                             tm_k, tm_v, partial, head_dim, plan, work, token_major ? 1 : 0, status);
+    return launch_overlapped(kv_partial_tc_kernel<NBOX, FUSED>, dim3(work.n_chunks),
+                             dim3(FUSED ? kKvThreadsFused : kKvThreads), L::smem_bytes, stream, tm_k, tm_v, partial,
+                             head_dim, plan, work, token_major ? 1 : 0, status, pa, tm_cos, tm_sin);
 }
 
 template <int C>
@@ -460,11 +590,18 @@ cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float*
 
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
                                  int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const ProducerArgs* producer, const CUtensorMap* tm_tables) {
     (void)n_tokens;
-    if (head_dim_atoms(head_dim) == 1)
-        return launch_tc<1>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream);
-    return launch_tc<2>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream);
+    const ProducerArgs pa = producer ? *producer : ProducerArgs{nullptr, nullptr, nullptr, nullptr, 0};
+    const CUtensorMap none{};
+    const CUtensorMap& tc = tm_tables ? tm_tables[0] : none;
+    const CUtensorMap& ts = tm_tables ? tm_tables[1] : none;
+    const bool one = head_dim_atoms(head_dim) == 1;
+    if (producer)
+        return one ? launch_tc<1, true>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
+                   : launch_tc<2, true>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts);
+    return one ? launch_tc<1, false>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
+               : launch_tc<2, false>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts);
 }
 
 cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float* partial, int64_t n_tokens,
@@ -484,10 +621,12 @@ cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides
 }
 
 cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
-                               const KvPlan& plan, cudaStream_t stream) {
+                               const KvPlan& plan, cudaStream_t stream, const ProducerArgs* producer) {
     dim3 grid((head_dim + 31) / 32, head_dim / 8, hc);
+    const double* kp = producer ? producer->ksum_partial : nullptr;
+    float* ks = producer ? producer->ksum : nullptr;
     return launch_overlapped(kv_finalize_kernel, grid, dim3(256), 0, stream, partial, kv, kv_image, h0, head_dim,
-                             plan);
+                             plan, kp, ks);
 }
 
 }  // namespace la

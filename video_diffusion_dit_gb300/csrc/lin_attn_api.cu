@@ -22,6 +22,8 @@ struct lin_attn_ctx {
     float* kv = nullptr;          // [heads][D][D] FP32 reduced KV
     uint8_t* kv_image = nullptr;  // [heads] x three-term BF16 image for the tensor-core apply
     int* status = nullptr;        // device status word (LIN_ATTN_ERR_TIMEOUT if a kernel gave up)
+    double* ksum_partial = nullptr;  // fused path: [heads][seg_stride_alloc][8][D] FP64 column sums of relu(K)
+    float* ksum = nullptr;           // fused path: [heads][D] FP32 reduced column sums
     // host-buffer path staging, allocated on first use
     void* st_q = nullptr;
     void* st_k = nullptr;
@@ -116,11 +118,29 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     return LIN_ATTN_OK;
 }
 
+// 2-D map over an FP32 [rows][cols] table (cols * 4 a multiple of 16), box (cols, box_rows),
+// no swizzle: a box lands in shared memory as box_rows dense rows of cols floats.
+int make_map_2d_f32(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (table) failed (CUresult %d)", (int)r);
+    return LIN_ATTN_OK;
+}
+
 void free_all(lin_attn_ctx* c) {
     cudaFree(c->partial);
     cudaFree(c->kv);
     cudaFree(c->kv_image);
     cudaFree(c->status);
+    cudaFree(c->ksum_partial);
+    cudaFree(c->ksum);
     cudaFree(c->st_q);
     cudaFree(c->st_k);
     cudaFree(c->st_v);
@@ -152,7 +172,8 @@ int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void
 // brackets the stages.
 int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
                   int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream, int h0, int hc,
-                  cudaEvent_t* ev, int layout = LIN_ATTN_LAYOUT_HND) {
+                  cudaEvent_t* ev, int layout = LIN_ATTN_LAYOUT_HND, const float* rope_cos = nullptr,
+                  const float* rope_sin = nullptr) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
     const bool tc = mode == LIN_ATTN_MODE_HIGH;
@@ -170,6 +191,12 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
     float* kv_h0 = c->kv + h0 * dd;
     uint8_t* image_h0 = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
     cudaError_t e;
+    // Fused producer step: the KV kernel and the reduction index the column sums by layer
+    // head, the apply by the launch's own heads.
+    const bool fused = rope_cos != nullptr;
+    const la::ProducerArgs pa_kv{rope_cos, rope_sin, c->ksum_partial, c->ksum, static_cast<int>(n_tokens)};
+    const la::ProducerArgs pa_apply{rope_cos, rope_sin, c->ksum_partial, c->ksum + static_cast<size_t>(h0) * D,
+                                    static_cast<int>(n_tokens)};
 
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (tc) {
@@ -178,7 +205,15 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         if (rc) return rc;
         rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile, tm, H);
         if (rc) return rc;
-        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, c->status, stream);
+        CUtensorMap tabs[2];
+        if (fused) {
+            for (int t = 0; t < 2; ++t) {
+                rc = make_map_2d_f32(&tabs[t], t ? rope_sin : rope_cos, D / 2, n_tokens, la::kKvTile);
+                if (rc) return rc;
+            }
+        }
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, c->status, stream,
+                                     fused ? &pa_kv : nullptr, fused ? tabs : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
     } else {
         e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), sd,
@@ -186,7 +221,8 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    e = la::launch_kv_finalize(c->partial, c->kv, tc ? c->kv_image : nullptr, h0, hc, D, plan, stream);
+    e = la::launch_kv_finalize(c->partial, c->kv, tc ? c->kv_image : nullptr, h0, hc, D, plan, stream,
+                               fused ? &pa_kv : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     if (tc) {
@@ -196,7 +232,8 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
                       : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
         if (rc) return rc;
-        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream);
+        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream,
+                                fused ? &pa_apply : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     } else {
         e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), sd, kv_h0, den, out, hc, n_tokens, D, bf16_out,
@@ -290,7 +327,10 @@ int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int h
     bool good = cudaMalloc(&c->partial, sizeof(float) * dd * heads * c->seg_stride_alloc) == cudaSuccess &&
                 cudaMalloc(&c->kv, sizeof(float) * dd * heads) == cudaSuccess &&
                 cudaMalloc(&c->kv_image, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads) == cudaSuccess &&
-                cudaMalloc(&c->status, sizeof(int)) == cudaSuccess;
+                cudaMalloc(&c->status, sizeof(int)) == cudaSuccess &&
+                cudaMalloc(&c->ksum_partial, sizeof(double) * heads * c->seg_stride_alloc * 8 * head_dim) ==
+                    cudaSuccess &&
+                cudaMalloc(&c->ksum, sizeof(float) * heads * head_dim) == cudaSuccess;
     if (!good) {
         cudaGetLastError();
         free_all(c);
@@ -347,6 +387,26 @@ int lin_attn_forward_layout(lin_attn_ctx* ctx, const void* q_rot, const void* k_
     ctx->n_events = 0;
     return enqueue_heads(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode,
                          reinterpret_cast<cudaStream_t>(stream), 0, ctx->heads, ev, layout);
+}
+
+int lin_attn_forward_fused(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* rope_cos,
+                           const float* rope_sin, void* out, int out_dtype, int64_t n_tokens, int mode,
+                           struct CUstream_st* stream) {
+    if (!rope_cos || !rope_sin) return fail(LIN_ATTN_ERR_INVALID_ARG, "rotation table pointer is NULL");
+    // check_call wants a denominator pointer; the fused call forms the denominators itself.
+    int rc = check_call(ctx, q, k, v, rope_cos, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    if (mode != LIN_ATTN_MODE_HIGH)
+        return fail(LIN_ATTN_ERR_UNSUPPORTED, "the fused producer step runs in LIN_ATTN_MODE_HIGH only");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
+        !aligned16(out))
+        return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    cudaEvent_t* ev = ctx->n_events == 4 ? ctx->events : nullptr;
+    ctx->n_events = 0;
+    return enqueue_heads(ctx, q, k, v, nullptr, out, out_dtype, n_tokens, mode, reinterpret_cast<cudaStream_t>(stream),
+                         0, ctx->heads, ev, LIN_ATTN_LAYOUT_HND, rope_cos, rope_sin);
 }
 
 int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,

@@ -3,7 +3,10 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include "ptx.cuh"
 
 namespace la {
 
@@ -119,15 +122,77 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The producer step fused into the tensor-core kernels (ReLU + interleaved RoPE on the
+// loaded Q / K tiles, the normaliser from the activated un-rotated copies).
+//   cos, sin : FP32 [N][D/2] rotation tables (pair p of token n is turned by cos/sin[n][p])
+//   ksum_partial : FP64 [H][seg_stride][8][D] per-chunk, per-row-group column sums of
+//                  relu(K) (scratch)
+//   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
+struct ProducerArgs {
+    const float* cos;
+    const float* sin;
+    double* ksum_partial;
+    float* ksum;
+    int n_tokens;
+};
+// Added to every normaliser denominator (den = relu(q) . sum relu(k) + kDenEps).
+constexpr float kDenEps = 1e-6f;
+
+// Producer step on one 16-byte chunk (8 BF16 values = 4 rotation pairs) of a Q or K row:
+// ReLU, then each pair (x0, x1) is turned by (c, s) as (x0 c - x1 s, x0 s + x1 c) with
+// binary32 products and sums in exactly this order (no fused multiply-add), rounded once to
+// BF16 (nearest-even).  The activated (un-rotated) values are returned in `act` for the
+// normaliser.
+__device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const float4 s4, float (&act)[8]) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t outw[4];
+    const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+    const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float x0 = fmaxf(__uint_as_float(in[j] << 16), 0.f);
+        const float x1 = fmaxf(__uint_as_float(in[j] & 0xFFFF0000u), 0.f);
+        act[2 * j] = x0;
+        act[2 * j + 1] = x1;
+        const float y0 = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
+        const float y1 = __fadd_rn(__fmul_rn(x0, sn[j]), __fmul_rn(x1, cs[j]));
+        const __nv_bfloat162 y = __floats2bfloat162_rn(y0, y1);
+        outw[j] = *reinterpret_cast<const uint32_t*>(&y);
+    }
+    w = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+}
+
+// Rotation-table rows of one 8-row batch of the producer transform: rows row0 + rg + 8k,
+// k = 0..7, columns 8c..8c+7 (pairs 4c..4c+3).  Rows past the end (or dead chunks) get
+// zeros.  Issued a batch ahead of use so the L2 latency overlaps the transform.
+__device__ __forceinline__ void load_rope_rows(const float* cos, const float* sin, int64_t pairs, int c, int row0,
+                                               int rg, int n_tokens, bool live, uint64_t pol, float4 (&cv)[8],
+                                               float4 (&sv)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int n = row0 + rg + 8 * k;
+        if (live && n < n_tokens) {
+            cv[k] = ldg_f4_hint(cos + n * pairs + 4 * c, pol);
+            sv[k] = ldg_f4_hint(sin + n * pairs + 4 * c, pol);
+        } else {
+            cv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            sv[k] = cv[k];
+        }
+    }
+}
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  `partial` is the base of the layer's
 // [H][seg_stride][D][D] partial buffer (head 0); the K/V maps/pointers start at head h0.
 
 // KV partial sums on tensor cores (BF16 x BF16 -> FP32).  The tensor maps index
 // (column, token, head) or, if token_major, (column, head, token).
+// With `producer` (fused path) tm_tables holds the maps of the two rotation tables (2-D,
+// (D/2, N), box (D/2, 64), no swizzle).
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
                                  int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const ProducerArgs* producer = nullptr,
+                                 const CUtensorMap* tm_tables = nullptr);
 
 // KV partial sums with FP32 FMA on CUDA cores (operands upcast from BF16).
 cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides st, float* partial, int64_t n_tokens,
@@ -137,12 +202,13 @@ cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides
 // kv[h][i][j] (FP32) and, if kv_image != nullptr, its three-term BF16 image for the
 // tensor-core apply.  kv / kv_image are the layer's base pointers (head 0).
 cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
-                               const KvPlan& plan, cudaStream_t stream);
+                               const KvPlan& plan, cudaStream_t stream, const ProducerArgs* producer = nullptr);
 
 // out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms (maps as above).
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, cudaStream_t stream);
+                            bool token_major, int grid, int* status, cudaStream_t stream,
+                            const ProducerArgs* producer = nullptr);
 
 // out = (Q . KV) * (1 / den) with FP32 FMA on CUDA cores; Q and out share the strides.
 cudaError_t launch_apply_ffma(const uint16_t* q, Strides st, const float* kv, const float* den, void* out, int heads,

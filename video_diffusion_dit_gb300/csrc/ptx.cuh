@@ -104,6 +104,21 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+// L2 policy for small data every CTA re-reads (rotation tables): kept in L2 last.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// 16-byte read-only global load with an L2 cache policy.
+__device__ __forceinline__ float4 ldg_f4_hint(const float* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // TMA loads / stores with an L2 cache policy (from createpolicy).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
                                                  int z, uint64_t pol) {
@@ -111,6 +126,14 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], "
         "[%2], %6;" ::"r"(dst),
         "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], "
+        "[%2], %5;" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y), "l"(pol)
         : "memory");
 }
 __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, uint32_t src, int x, int y, int z, uint64_t pol) {
