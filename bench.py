@@ -324,8 +324,7 @@ def run_ours(args, w, world, rank, local, dist):
     peak, peak_kind = load_peaks()
     dom = max(("kv_partial", "apply"), key=lambda k: stage_ms[k])
     achieved = nbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
-    kernel_names = {"kv_partial": "kv_partial_tc_kernel" if args.mode == "high" else "kv_partial_ffma_kernel",
-                    "apply": "apply_tc_kernel" if args.mode == "high" else "apply_ffma_kernel"}
+    kernel_names = {"kv_partial": "kv_partial_tc_kernel", "apply": "apply_tc_kernel"}
     result = None
     if rank == 0:
         cpu = cpu_baseline(layer_to_numpy(layer), H, N, args.cpu_budget) if (world == 1 and not args.no_cpu) else None

@@ -18,7 +18,11 @@
  *   LIN_ATTN_MODE_HIGH      first GEMM on BF16 operands, FP32 accumulation and output;
  *                           second GEMM at FP32 accuracy (here: Q . (KV_hi + KV_mid + KV_lo)
  *                           with KV split into three BF16 terms, FP32 accumulation).
- *   LIN_ATTN_MODE_LOSSLESS  Q, K, V upcast to FP32 before both GEMMs (FP32 FMA on CUDA cores).
+ *   LIN_ATTN_MODE_LOSSLESS  the FP32 chain: Q, K, V upcast to FP32 before both GEMMs.  The
+ *                           inputs are BF16, so every product is exact in FP32 either way and
+ *                           this tier runs the same tensor-core kernels, with the first GEMM's
+ *                           tensor-core sums promoted into IEEE FP32 registers every 64 tokens
+ *                           (every 256 in 'high').
  * Both tiers have the same exact result; they differ only in rounding.
  *
  * Conventions shared by every entry point:
@@ -165,9 +169,10 @@ int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
  * tile) sequence, heads outermost, is cut into `*chunks` equal contiguous chunks (one CTA
  * each); every chunk leaves one partial D x D sum per head it touches, and each head's
  * partials (at most `*max_segments` for the busiest head) are added in a fixed pairwise
- * order.  The split depends on (heads, n_tokens, mode) only - never on the GPU - which is
- * what makes the summation order, and so the result, reproducible.  Either out-pointer
- * may be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad arguments.
+ * order.  The split depends on (heads, n_tokens) only - never on the GPU - which is what
+ * makes the summation order, and so the result, reproducible (both tiers use the same
+ * split).  Either out-pointer may be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad
+ * arguments.
  */
 int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *max_segments);
 

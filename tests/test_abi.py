@@ -88,14 +88,14 @@ def test_kv_plan_depends_on_shape_and_tier_only(la):
         for N in (1, 63, 64, 65, 256, 1000, 32760, 180320, 262144):
             if H * N >= 2 ** 31:
                 continue
-            for mode, target in (("high", 152), ("lossless", 608)):
+            for mode, target in (("high", 152), ("lossless", 152)):
                 G, segs = la.kv_plan(H, N, mode)
                 assert (G, segs) == la.kv_plan(H, N, mode)
                 T = H * -(-N // 64)
                 assert G == min(target, T, 150 * H)
                 assert 1 <= segs <= -(-G // H) + 1 <= 160
     assert la.kv_plan(20, 180320, "high") == (152, 9)
-    assert la.kv_plan(20, 180320, "lossless") == (608, 32)
+    assert la.kv_plan(20, 180320, "lossless") == (152, 9)
     with pytest.raises(la.LinAttnError):
         la.kv_plan(0, 10, "high")
 

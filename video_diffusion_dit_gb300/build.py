@@ -53,7 +53,7 @@ def build(verbose_ptxas: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), "-shared", *GENCODE, "-o", tmp, *objs]
+    cmd = [nvcc(), "-shared", *GENCODE, "-Xlinker", "--no-undefined", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

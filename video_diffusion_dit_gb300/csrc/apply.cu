@@ -353,101 +353,6 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     }
 }
 
-// ============================================================================ CUDA cores
-// 'lossless': Q upcast to FP32 (exact), FP32 FMA against KV held in shared memory.
-// Persistent blocks over contiguous ranges of 64-token tiles; thread (tn, tj) owns tokens
-// 4tn..4tn+3 and columns tj + 16b.  Sums run over i in ascending order.
-constexpr int kFfmaTile = 64;
-
-__host__ __device__ inline size_t apply_ffma_smem_bytes(int head_dim) {
-    return (static_cast<size_t>(head_dim) * head_dim + static_cast<size_t>(kFfmaTile) * (head_dim + 1)) *
-           sizeof(float);
-}
-
-template <int C, bool OUT_BF16>
-__global__ void __launch_bounds__(256) apply_ffma_kernel(const uint16_t* __restrict__ q, const Strides sd,
-                                                         const float* __restrict__ kv, const float* __restrict__ den,
-                                                         void* __restrict__ out, int heads, int n_tokens,
-                                                         int tiles_per_head) {
-    constexpr int D = 16 * C;
-    extern __shared__ float sm[];
-    float* kvs = sm;           // [D][D]
-    float* qt = sm + D * D;    // [D][kFfmaTile] (transposed Q tile), reused as [kFfmaTile][D + 1] output
-    const int total = heads * tiles_per_head;
-    const int t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-    const int t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
-    const int tn = threadIdx.x & 15, tj = threadIdx.x >> 4;
-    int cur_h = -1;
-    for (int t = t_begin; t < t_end; ++t) {
-        const int h = t / tiles_per_head;
-        const int n0 = (t % tiles_per_head) * kFfmaTile;
-        const int rows = min(kFfmaTile, n_tokens - n0);
-        const int64_t row_base = static_cast<int64_t>(h) * n_tokens + n0;    // den index of row 0
-        const int64_t elem_base = h * sd.head + static_cast<int64_t>(n0) * sd.token;  // Q / out offset of row 0
-        __syncthreads();
-        if (h != cur_h) {
-            const float4* src = reinterpret_cast<const float4*>(kv + static_cast<int64_t>(h) * D * D);
-            for (int idx = threadIdx.x; idx < D * D / 4; idx += 256) reinterpret_cast<float4*>(kvs)[idx] = src[idx];
-            cur_h = h;
-        }
-        for (int idx = threadIdx.x; idx < kFfmaTile * (D / 8); idx += 256) {
-            const int r = idx % kFfmaTile, c = idx / kFfmaTile;
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < rows) w = *reinterpret_cast<const uint4*>(q + elem_base + r * sd.token + 8 * c);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                qt[(8 * c + 2 * e) * kFfmaTile + r] = __uint_as_float(ww[e] << 16);
-                qt[(8 * c + 2 * e + 1) * kFfmaTile + r] = __uint_as_float(ww[e] & 0xFFFF0000u);
-            }
-        }
-        __syncthreads();
-        float acc[4][C];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < C; ++b) acc[a][b] = 0.f;
-        for (int i = 0; i < D; ++i) {
-            const float4 qv = *reinterpret_cast<const float4*>(qt + i * kFfmaTile + 4 * tn);
-            float kr[C];
-#pragma unroll
-            for (int b = 0; b < C; ++b) kr[b] = kvs[i * D + tj + 16 * b];
-#pragma unroll
-            for (int b = 0; b < C; ++b) {
-                acc[0][b] = fmaf(qv.x, kr[b], acc[0][b]);
-                acc[1][b] = fmaf(qv.y, kr[b], acc[1][b]);
-                acc[2][b] = fmaf(qv.z, kr[b], acc[2][b]);
-                acc[3][b] = fmaf(qv.w, kr[b], acc[3][b]);
-            }
-        }
-        __syncthreads();
-        float* ys = qt;  // [kFfmaTile][D + 1]
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int r = 4 * tn + a;
-            const float rcp = r < rows ? __frcp_rn(den[row_base + r]) : 0.f;
-#pragma unroll
-            for (int b = 0; b < C; ++b) ys[r * (D + 1) + tj + 16 * b] = acc[a][b] * rcp;
-        }
-        __syncthreads();
-        if (!OUT_BF16) {
-            float* o = reinterpret_cast<float*>(out) + elem_base;
-            for (int idx = threadIdx.x; idx < rows * D; idx += 256) {
-                const int r = idx / D, c = idx % D;
-                o[r * sd.token + c] = ys[r * (D + 1) + c];
-            }
-        } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + elem_base;
-            for (int idx = threadIdx.x; idx < rows * D / 2; idx += 256) {
-                const int e = 2 * idx;
-                const int r = e / D, c = e % D;
-                *reinterpret_cast<__nv_bfloat162*>(o + r * sd.token + c) =
-                    __floats2bfloat162_rn(ys[r * (D + 1) + c], ys[r * (D + 1) + c + 1]);
-            }
-        }
-    }
-}
-
 template <int NBOX, bool BF16, bool FUSED>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
                       int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
@@ -474,36 +379,6 @@ cudaError_t launch_tc_any(const CUtensorMap& tm_q, const CUtensorMap& tm_out, co
                                         stream, none);
 }
 
-template <int C, bool BF16>
-cudaError_t launch_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
-                        int n_tokens, int grid, cudaStream_t stream) {
-    const size_t smem = apply_ffma_smem_bytes(16 * C);
-    cudaError_t e = cudaFuncSetAttribute(apply_ffma_kernel<C, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int tph = (n_tokens + kFfmaTile - 1) / kFfmaTile;
-    const int total = heads * tph;
-    if (grid > total) grid = total;
-    apply_ffma_kernel<C, BF16><<<grid, 256, smem, stream>>>(q, sd, kv, den, out, heads, n_tokens, tph);
-    return cudaGetLastError();
-}
-
-template <bool BF16>
-cudaError_t dispatch_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
-                          int n_tokens, int head_dim, int grid, cudaStream_t stream) {
-    switch (head_dim / 16) {
-        case 1: return launch_ffma<1, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 2: return launch_ffma<2, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 3: return launch_ffma<3, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 4: return launch_ffma<4, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 5: return launch_ffma<5, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 6: return launch_ffma<6, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 7: return launch_ffma<7, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        case 8: return launch_ffma<8, BF16>(q, sd, kv, den, out, heads, n_tokens, grid, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
@@ -519,13 +394,6 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
                         : launch_tc_any<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer);
     return out_bf16 ? launch_tc_any<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer)
                     : launch_tc_any<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer);
-}
-
-cudaError_t launch_apply_ffma(const uint16_t* q, Strides sd, const float* kv, const float* den, void* out, int heads,
-                              int64_t n_tokens, int head_dim, bool out_bf16, int grid, cudaStream_t stream) {
-    const int n = static_cast<int>(n_tokens);
-    return out_bf16 ? dispatch_ffma<true>(q, sd, kv, den, out, heads, n, head_dim, grid, stream)
-                    : dispatch_ffma<false>(q, sd, kv, den, out, heads, n, head_dim, grid, stream);
 }
 
 }  // namespace la

@@ -5,6 +5,10 @@
 // accumulation/output ('high'); the model's fallback chain upcasts both operands to FP32
 // first ('lossless').
 //
+// Both tiers run on tensor cores: BF16 x BF16 products are exact in FP32, so the first
+// GEMM on BF16 operands is the FP32 GEMM on the upcast operands up to rounding; 'lossless'
+// promotes the tensor-core sums into FP32 registers four times as often.
+//
 // Work split (KvPlan): the layer's (head, 64-token tile) sequence is cut into G equal
 // contiguous chunks, one CTA each.  A chunk leaves one D x D partial sum per head it
 // touches (a "segment"); kv_finalize adds each head's partials in a fixed pairwise order.
@@ -26,7 +30,10 @@ namespace {
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
 constexpr int kKvThreadsFused = 320;  // + warps 6..9: the producer-step transform
-constexpr int kKvPromoteTiles = 4;  // tiles per tensor-core sub-chunk (256 tokens)
+// Tiles per tensor-core sub-chunk before its sum is promoted into FP32 registers: 4 (256
+// tokens) in the 'high' tier, 1 (64 tokens) in the 'lossless' tier.
+constexpr int kPromoteHigh = 4;
+constexpr int kPromoteLossless = 1;
 constexpr uint32_t kKvAtomBytes = kKvTile * 128;  // one box: 64 token rows x 128 bytes
 
 template <int NBOX, bool FUSED>
@@ -54,7 +61,7 @@ __device__ __forceinline__ ChunkTiles chunk_tiles(const KvPlan& plan, const KvLa
     return r;
 }
 
-template <int NBOX, bool FUSED>
+template <int NBOX, bool FUSED, int PROMOTE>
 __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     kv_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          float* __restrict__ partial, int head_dim, const KvPlan plan, const KvLaunch work,
@@ -170,16 +177,16 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         if (lane == 0) {
             // ---------------- MMA issuer
             // Each segment (the chunk's tiles of one head) is accumulated in sub-chunks of
-            // kKvPromoteTiles tiles, alternating between two TMEM accumulators; the epilogue
+            // PROMOTE tiles, alternating between two TMEM accumulators; the epilogue
             // adds every finished sub-chunk into FP32 registers (round-to-nearest), so
-            // tensor-core accumulation never runs over more than 256 tokens.
+            // tensor-core accumulation never runs over more than PROMOTE * 64 tokens.
             constexpr uint32_t idesc = make_idesc_bf16_f32(128, 64 * NBOX, true, true);
             uint32_t it = 0, sub = 0;
             bool ok = true;
             for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
                 const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
-                for (int64_t k0 = t; ok && k0 < seg_end; k0 += kKvPromoteTiles, ++sub) {
-                    const int64_t k1 = min(k0 + kKvPromoteTiles, seg_end);
+                for (int64_t k0 = t; ok && k0 < seg_end; k0 += PROMOTE, ++sub) {
+                    const int64_t k1 = min(k0 + PROMOTE, seg_end);
                     const uint32_t buf = sub & 1u;
                     if (!mbar_wait(acc_empty0 + 8u * buf, ((sub >> 1) & 1u) ^ 1u, abort_flag, status)) {
                         ok = false;
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             float acc[64 * NBOX];
 #pragma unroll
             for (int c = 0; c < 64 * NBOX; ++c) acc[c] = 0.f;
-            for (int64_t k0 = t; k0 < seg_end; k0 += kKvPromoteTiles, ++sub) {
+            for (int64_t k0 = t; k0 < seg_end; k0 += PROMOTE, ++sub) {
                 const uint32_t buf = sub & 1u;
                 if (!mbar_wait(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status)) {
                     ok = false;
@@ -331,94 +338,6 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
-    }
-}
-
-// ============================================================================ CUDA cores
-// 'lossless': both operands upcast from BF16 to FP32 (exact), FP32 FMA.  One CTA per chunk;
-// thread (ti, tj) owns KV rows ti + 16a and columns tj + 16b of the running segment sum;
-// tokens are added in ascending order, 32 at a time through shared memory, into a sum
-// that is folded into the segment total every 256 tokens.
-constexpr int kFfmaKvRows = 32;
-constexpr int kFfmaPromoteRows = 256;
-
-template <int C>
-__global__ void __launch_bounds__(256) kv_partial_ffma_kernel(const uint16_t* __restrict__ k,
-                                                              const uint16_t* __restrict__ v, const Strides sd,
-                                                              float* __restrict__ partial, int n_tokens,
-                                                              const KvPlan plan, const KvLaunch work) {
-    constexpr int D = 16 * C;
-    __shared__ float ks[kFfmaKvRows][D];
-    __shared__ float vs[kFfmaKvRows][D];
-    const ChunkTiles ct = chunk_tiles(plan, work);
-    const int64_t tph = plan.tiles_per_head;
-    const int ti = threadIdx.x & 15, tj = threadIdx.x >> 4;
-
-    for (int64_t t = ct.t_s; t < ct.t_e;) {
-        const int h = static_cast<int>(t / tph);
-        const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
-        const int n_begin = static_cast<int>((t % tph) * kKvTile);
-        const int n_end = static_cast<int>(min(static_cast<int64_t>(n_tokens), (seg_end - h * tph) * kKvTile));
-        const uint16_t* kh = k + static_cast<int64_t>(h - work.h0) * sd.head;
-        const uint16_t* vh = v + static_cast<int64_t>(h - work.h0) * sd.head;
-
-        // Two-level FP32 sum: `acc` runs over at most kFfmaPromoteRows tokens, then is
-        // added into the segment total `tot` (keeps the rounding error of long segments down).
-        float acc[C][C], tot[C][C];
-#pragma unroll
-        for (int a = 0; a < C; ++a)
-#pragma unroll
-            for (int b = 0; b < C; ++b) acc[a][b] = tot[a][b] = 0.f;
-
-        for (int n0 = n_begin; n0 < n_end; n0 += kFfmaKvRows) {
-            if (n0 != n_begin && (n0 - n_begin) % kFfmaPromoteRows == 0) {
-#pragma unroll
-                for (int a = 0; a < C; ++a)
-#pragma unroll
-                    for (int b = 0; b < C; ++b) {
-                        tot[a][b] += acc[a][b];
-                        acc[a][b] = 0.f;
-                    }
-            }
-            const int rows = min(kFfmaKvRows, n_end - n0);
-            __syncthreads();
-            for (int idx = threadIdx.x; idx < kFfmaKvRows * (D / 8); idx += 256) {
-                const int r = idx / (D / 8), c = idx % (D / 8);
-                uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
-                if (r < rows) {
-                    kw = *reinterpret_cast<const uint4*>(kh + static_cast<int64_t>(n0 + r) * sd.token + 8 * c);
-                    vw = *reinterpret_cast<const uint4*>(vh + static_cast<int64_t>(n0 + r) * sd.token + 8 * c);
-                }
-                const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
-                const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    ks[r][8 * c + 2 * e] = __uint_as_float(kk[e] << 16);
-                    ks[r][8 * c + 2 * e + 1] = __uint_as_float(kk[e] & 0xFFFF0000u);
-                    vs[r][8 * c + 2 * e] = __uint_as_float(vv[e] << 16);
-                    vs[r][8 * c + 2 * e + 1] = __uint_as_float(vv[e] & 0xFFFF0000u);
-                }
-            }
-            __syncthreads();
-            for (int r = 0; r < rows; ++r) {
-                float kr[C], vr[C];
-#pragma unroll
-                for (int a = 0; a < C; ++a) kr[a] = ks[r][ti + 16 * a];
-#pragma unroll
-                for (int b = 0; b < C; ++b) vr[b] = vs[r][tj + 16 * b];
-#pragma unroll
-                for (int a = 0; a < C; ++a)
-#pragma unroll
-                    for (int b = 0; b < C; ++b) acc[a][b] = fmaf(kr[a], vr[b], acc[a][b]);
-            }
-        }
-        const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
-        float* dst = partial + slot * D * D;
-#pragma unroll
-        for (int a = 0; a < C; ++a)
-#pragma unroll
-            for (int b = 0; b < C; ++b) dst[(ti + 16 * a) * D + tj + 16 * b] = tot[a][b] + acc[a][b];
-        t = seg_end;
     }
 }
 
@@ -566,58 +485,37 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
     *reinterpret_cast<uint4*>(img + 2 * term_bytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-template <int NBOX, bool FUSED>
+template <int NBOX, bool FUSED, int PROMOTE>
 cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int head_dim,
                       const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, cudaStream_t stream,
                       const ProducerArgs& pa, const CUtensorMap& tm_cos, const CUtensorMap& tm_sin) {
     using L = KvLayout<NBOX, FUSED>;
-    cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX, FUSED>,
+    cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX, FUSED, PROMOTE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_overlapped(kv_partial_tc_kernel<NBOX, FUSED>, dim3(work.n_chunks),
+    return launch_overlapped(kv_partial_tc_kernel<NBOX, FUSED, PROMOTE>, dim3(work.n_chunks),
                              dim3(FUSED ? kKvThreadsFused : kKvThreads), L::smem_bytes, stream, tm_k, tm_v, partial,
                              head_dim, plan, work, token_major ? 1 : 0, status, pa, tm_cos, tm_sin);
-}
-
-template <int C>
-cudaError_t launch_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float* partial, int n_tokens,
-                        const KvPlan& plan, const KvLaunch& work, cudaStream_t stream) {
-    kv_partial_ffma_kernel<C><<<work.n_chunks, 256, 0, stream>>>(k, v, sd, partial, n_tokens, plan, work);
-    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
-                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
-                                 cudaStream_t stream, const ProducerArgs* producer, const CUtensorMap* tm_tables) {
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major,
+                                 bool lossless, int* status, cudaStream_t stream, const ProducerArgs* producer,
+                                 const CUtensorMap* tm_tables) {
     (void)n_tokens;
     const ProducerArgs pa = producer ? *producer : ProducerArgs{nullptr, nullptr, nullptr, nullptr, 0};
     const CUtensorMap none{};
     const CUtensorMap& tc = tm_tables ? tm_tables[0] : none;
     const CUtensorMap& ts = tm_tables ? tm_tables[1] : none;
     const bool one = head_dim_atoms(head_dim) == 1;
-    if (producer)
-        return one ? launch_tc<1, true>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
-                   : launch_tc<2, true>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts);
-    return one ? launch_tc<1, false>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
-               : launch_tc<2, false>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts);
-}
-
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides sd, float* partial, int64_t n_tokens,
-                                   int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream) {
-    const int n = static_cast<int>(n_tokens);
-    switch (head_dim / 16) {
-        case 1: return launch_ffma<1>(k, v, sd, partial, n, plan, work, stream);
-        case 2: return launch_ffma<2>(k, v, sd, partial, n, plan, work, stream);
-        case 3: return launch_ffma<3>(k, v, sd, partial, n, plan, work, stream);
-        case 4: return launch_ffma<4>(k, v, sd, partial, n, plan, work, stream);
-        case 5: return launch_ffma<5>(k, v, sd, partial, n, plan, work, stream);
-        case 6: return launch_ffma<6>(k, v, sd, partial, n, plan, work, stream);
-        case 7: return launch_ffma<7>(k, v, sd, partial, n, plan, work, stream);
-        case 8: return launch_ffma<8>(k, v, sd, partial, n, plan, work, stream);
-        default: return cudaErrorInvalidValue;
-    }
+#define LA_KV_LAUNCH(NB, FU, PR) \
+    launch_tc<NB, FU, PR>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
+    if (producer) return one ? LA_KV_LAUNCH(1, true, kPromoteHigh) : LA_KV_LAUNCH(2, true, kPromoteHigh);
+    if (lossless) return one ? LA_KV_LAUNCH(1, false, kPromoteLossless) : LA_KV_LAUNCH(2, false, kPromoteLossless);
+    return one ? LA_KV_LAUNCH(1, false, kPromoteHigh) : LA_KV_LAUNCH(2, false, kPromoteHigh);
+#undef LA_KV_LAUNCH
 }
 
 cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,

@@ -176,9 +176,9 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                   const float* rope_sin = nullptr) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
-    const bool tc = mode == LIN_ATTN_MODE_HIGH;
+    const bool lossless = mode == LIN_ATTN_MODE_LOSSLESS;
     const bool tm = layout == LIN_ATTN_LAYOUT_NHD;  // token-major activations
-    const la::KvPlan plan = la::kv_plan(H, n_tokens, tc);
+    const la::KvPlan plan = la::kv_plan(H, n_tokens);
     const la::KvLaunch work = la::kv_launch(plan, h0, hc);
     const la::Strides sd = tm ? la::Strides{D, static_cast<int64_t>(H) * D}
                               : la::Strides{static_cast<int64_t>(n_tokens) * D, D};
@@ -188,7 +188,6 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
     v = static_cast<const uint16_t*>(v) + h0 * sd.head;
     den += h0 * static_cast<size_t>(n_tokens);
     out = static_cast<uint8_t*>(out) + h0 * sd.head * (bf16_out ? 2 : 4);
-    float* kv_h0 = c->kv + h0 * dd;
     uint8_t* image_h0 = c->kv_image + h0 * static_cast<size_t>(la::kv_image_bytes(D));
     cudaError_t e;
     // Fused producer step: the KV kernel and the reduction index the column sums by layer
@@ -199,7 +198,7 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                                     static_cast<int>(n_tokens)};
 
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (tc) {
+    {
         CUtensorMap tk, tv;
         int rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kKvTile, tm, H);
         if (rc) return rc;
@@ -212,20 +211,15 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                 if (rc) return rc;
             }
         }
-        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, c->status, stream,
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, lossless, c->status, stream,
                                      fused ? &pa_kv : nullptr, fused ? tabs : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
-    } else {
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), sd,
-                                       c->partial, n_tokens, D, plan, work, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "kv_partial_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    e = la::launch_kv_finalize(c->partial, c->kv, tc ? c->kv_image : nullptr, h0, hc, D, plan, stream,
-                               fused ? &pa_kv : nullptr);
+    e = la::launch_kv_finalize(c->partial, c->kv, c->kv_image, h0, hc, D, plan, stream, fused ? &pa_kv : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-    if (tc) {
+    {
         CUtensorMap tq, to;
         int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
         if (rc) return rc;
@@ -235,10 +229,6 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream,
                                 fused ? &pa_apply : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
-    } else {
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q), sd, kv_h0, den, out, hc, n_tokens, D, bf16_out,
-                                  2 * c->n_sms, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "apply_ffma launch");
     }
     if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     return ok();
@@ -280,7 +270,7 @@ const char* lin_attn_last_error(void) { return g_last_error.c_str(); }
 int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int* chunks, int* max_segments) {
     if (heads < 1 || n_tokens < 1 || (mode != LIN_ATTN_MODE_HIGH && mode != LIN_ATTN_MODE_LOSSLESS))
         return fail(LIN_ATTN_ERR_INVALID_ARG, "bad heads / n_tokens / mode");
-    const la::KvPlan p = la::kv_plan(heads, n_tokens, mode == LIN_ATTN_MODE_HIGH);
+    const la::KvPlan p = la::kv_plan(heads, n_tokens);
     int most = 0;
     for (int h = 0; h < heads; ++h) {
         const int n = la::segments_of_head(p, h);

@@ -18,10 +18,9 @@ constexpr int kApplyTile = 128;
 // Work chunks of the KV reduction.  The layer's (head, 64-token tile) sequence, heads
 // outermost, is cut into G equal contiguous chunks; each chunk is summed by one CTA and
 // leaves one partial KV per head it touches.  G is a constant of the kernel (152 = one
-// chunk per SM of a 152-SM part for the tensor-core kernel, four per SM for the CUDA-core
-// kernel), never read from the device, so the summation order is fixed by the shape.
-constexpr int kChunksTensorCore = 152;
-constexpr int kChunksCudaCore = 608;
+// chunk per SM of a 152-SM part), never read from the device, so the summation order is
+// fixed by the shape.
+constexpr int kChunks = 152;
 constexpr int kChunksPerHeadCap = 150;  // G <= 150 * H keeps a head under kMaxSegments partials
 constexpr int kMaxSegments = 160;       // partials per head the reduction can add
 
@@ -32,11 +31,11 @@ struct KvPlan {
     int seg_stride;          // partial slots per head: ceil(G / H) + 1 >= segments of any head
 };
 
-__host__ __device__ inline KvPlan kv_plan(int heads, int64_t n_tokens, bool tensor_cores) {
+__host__ __device__ inline KvPlan kv_plan(int heads, int64_t n_tokens) {
     KvPlan p;
     p.tiles_per_head = (n_tokens + kKvTile - 1) / kKvTile;
     p.total_tiles = p.tiles_per_head * heads;
-    int64_t g = tensor_cores ? kChunksTensorCore : kChunksCudaCore;
+    int64_t g = kChunks;
     if (g > p.total_tiles) g = p.total_tiles;
     if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
     p.chunks = static_cast<int>(g);
@@ -59,7 +58,7 @@ __host__ __device__ inline int segments_of_head(const KvPlan& p, int h) {
 }
 // Largest seg_stride any n_tokens can produce for `heads` (scratch sizing).
 __host__ __device__ inline int kv_seg_stride_bound(int heads) {
-    int64_t g = kChunksCudaCore > kChunksTensorCore ? kChunksCudaCore : kChunksTensorCore;
+    int64_t g = kChunks;
     if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
     return static_cast<int>((g + heads - 1) / heads + 1);
 }
@@ -186,17 +185,14 @@ __device__ __forceinline__ void load_rope_rows(const float* cos, const float* si
 // [H][seg_stride][D][D] partial buffer (head 0); the K/V maps/pointers start at head h0.
 
 // KV partial sums on tensor cores (BF16 x BF16 -> FP32).  The tensor maps index
-// (column, token, head) or, if token_major, (column, head, token).
+// (column, token, head) or, if token_major, (column, head, token).  `lossless` promotes
+// the tensor-core sums into FP32 registers every tile instead of every 4 tiles.
 // With `producer` (fused path) tm_tables holds the maps of the two rotation tables (2-D,
 // (D/2, N), box (D/2, 64), no swizzle).
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
-                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major, int* status,
-                                 cudaStream_t stream, const ProducerArgs* producer = nullptr,
+                                 int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major,
+                                 bool lossless, int* status, cudaStream_t stream, const ProducerArgs* producer = nullptr,
                                  const CUtensorMap* tm_tables = nullptr);
-
-// KV partial sums with FP32 FMA on CUDA cores (operands upcast from BF16).
-cudaError_t launch_kv_partial_ffma(const uint16_t* k, const uint16_t* v, Strides st, float* partial, int64_t n_tokens,
-                                   int head_dim, const KvPlan& plan, const KvLaunch& work, cudaStream_t stream);
 
 // Fixed-order pairwise reduction of each head's partials for heads [h0, h0 + hc):
 // kv[h][i][j] (FP32) and, if kv_image != nullptr, its three-term BF16 image for the
@@ -209,9 +205,5 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
                             bool token_major, int grid, int* status, cudaStream_t stream,
                             const ProducerArgs* producer = nullptr);
-
-// out = (Q . KV) * (1 / den) with FP32 FMA on CUDA cores; Q and out share the strides.
-cudaError_t launch_apply_ffma(const uint16_t* q, Strides st, const float* kv, const float* den, void* out, int heads,
-                              int64_t n_tokens, int head_dim, bool out_bf16, int grid, cudaStream_t stream);
 
 }  // namespace la

@@ -103,7 +103,7 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
             return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
 
     // Scratch carve-up: partials | KV | KV image | status word, each 256-byte aligned.
-    const la::KvPlan plan = la::kv_plan(heads, n_tokens, mode == LIN_ATTN_MODE_HIGH);
+    const la::KvPlan plan = la::kv_plan(heads, n_tokens);
     const la::KvLaunch work = la::kv_launch(plan, 0, heads);
     const size_t dd = static_cast<size_t>(head_dim) * head_dim;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -143,40 +143,24 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
     // Must start at zero: the status word, and the KV image (its padding columns are read
     // by the MMA and a previous call with another head dim may have left data there).
     if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-    if (mode == LIN_ATTN_MODE_HIGH && (e = cudaMemsetAsync(image, 0, image_bytes, s)) != cudaSuccess)
-        return cuda_fail(e, "cudaMemsetAsync");
+    if ((e = cudaMemsetAsync(image, 0, image_bytes, s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
 
-    if (mode == LIN_ATTN_MODE_HIGH) {
-        CUtensorMap tk, tv;
-        if (!make_map(&tk, k_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile) ||
-            !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
-            return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, false, status, s);
-    } else {
-        const la::Strides sd{n_tokens * head_dim, head_dim};
-        e = la::launch_kv_partial_ffma(static_cast<const uint16_t*>(k_rot), static_cast<const uint16_t*>(v), sd,
-                                       partial, n_tokens, head_dim, plan, work, s);
-    }
+    CUtensorMap tk, tv;
+    if (!make_map(&tk, k_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile) ||
+        !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
+        return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, false, mode == LIN_ATTN_MODE_LOSSLESS,
+                                 status, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_partial launch");
-    e = la::launch_kv_finalize(partial, kv, mode == LIN_ATTN_MODE_HIGH ? image : nullptr, 0, heads, head_dim, plan,
-                               s);
+    e = la::launch_kv_finalize(partial, kv, image, 0, heads, head_dim, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
-    if (mode == LIN_ATTN_MODE_HIGH) {
-        CUtensorMap tq, to;
-        const bool okq = make_map(&tq, q_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64,
-                                  la::kApplyTile);
-        const bool oko = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads,
-                                             64, 32)
-                                  : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, head_dim, n_tokens, heads,
-                                             32, 32);
-        if (!okq || !oko) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-        e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status,
-                                s);
-    } else {
-        const la::Strides sd{n_tokens * head_dim, head_dim};
-        e = la::launch_apply_ffma(static_cast<const uint16_t*>(q_rot), sd, kv, normalizer, out, heads, n_tokens,
-                                  head_dim, bf16_out, 2 * su.n_sms, s);
-    }
+    CUtensorMap tq, to;
+    const bool okq = make_map(&tq, q_rot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64,
+                              la::kApplyTile);
+    const bool oko = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, 32)
+                              : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, head_dim, n_tokens, heads, 32, 32);
+    if (!okq || !oko) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status, s);
     if (e != cudaSuccess) return cuda_fail(e, "apply launch");
     return la::record_error(LIN_ATTN_OK, "");
 }
