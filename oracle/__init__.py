@@ -68,6 +68,8 @@ def _bind(lib):
     lib.oracle_f32_to_bf16.restype = None
     lib.oracle_producer.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_double, p, p, p]
     lib.oracle_producer.restype = ctypes.c_int
+    lib.oracle_softmax_attention_rows.argtypes = [i64, i64, i64, p, p, p, ctypes.c_double, i64, p, p]
+    lib.oracle_softmax_attention_rows.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
@@ -200,6 +202,26 @@ def forward(q_bits, k_bits, v_bits, den, lib=None) -> np.ndarray:
                                         _ptr(den), _ptr(out))
     if rc:
         raise RuntimeError(f"oracle_forward failed ({rc})")
+    return out
+
+
+def softmax_attention_rows(q_bits, k_bits, v_bits, scale=None, rows=None, lib=None) -> np.ndarray:
+    """Softmax attention (no mask, default scale 1/sqrt(D)) for flat rows h*N + n: [len, D]."""
+    q_bits, k_bits, v_bits = _u16(q_bits), _u16(k_bits), _u16(v_bits)
+    H, N, D = _shape3(q_bits)
+    if k_bits.shape != (H, N, D) or v_bits.shape != (H, N, D):
+        raise ValueError("q, k, v shapes differ")
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    if rows is None:
+        n_rows, rows_ptr = H * N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows, rows_ptr = rows.size, _ptr(rows)
+    out = np.empty((n_rows, D), np.float64)
+    rc = (lib or load()).oracle_softmax_attention_rows(H, N, D, _ptr(q_bits), _ptr(k_bits), _ptr(v_bits), scale,
+                                                       n_rows, rows_ptr, _ptr(out))
+    if rc:
+        raise RuntimeError(f"oracle_softmax_attention_rows failed ({rc})")
     return out
 
 

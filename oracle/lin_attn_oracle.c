@@ -31,12 +31,20 @@
  * sum rounded to nearest), then rounded once to BF16 (nearest, ties to even), so that any
  * implementation following the same definition gets the same BF16 operands bit for bit.
  *
+ * The softmax anchor layer (oracle_softmax_attention_rows) follows the page "[sglang]
+ * SANA-Video 2.0 anchor attention의 FP32 upcast 제거로 720p 생성 52% 단축하기" (PR #49219),
+ * section 코드 분석, 2. GatedSoftmaxAttention: F.scaled_dot_product_attention(q, k, v,
+ * dropout_p=0.0) on [B, H, N, D] tensors - no mask, no dropout, default scale 1/sqrt(D):
+ *       out[h][n][j] = sum_m w_m v[h][m][j] / sum_m w_m,   w_m = exp(s_m - max_m s_m),
+ *       s_m = scale * sum_i q[h][n][i] k[h][m][i]
+ *
  * Arithmetic: every input value (BF16 bit patterns, FP32 denominators) is exact
  * in FP64; products and sums are FP64 in the order written (m ascending for KV,
  * i ascending for the apply).  Build with -ffp-contract=off and no fast-math so
  * the order stays as written.  Loops over independent outputs are split across
  * OpenMP threads; no output's arithmetic depends on the split.
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -214,6 +222,68 @@ int oracle_apply_rows(int64_t H, int64_t N, int64_t D, const uint16_t *q, const 
                 s += bf16_to_f64(qrow[i]) * kvh[i * D + j];
             out[r * D + j] = s / d;
         }
+    }
+    return bad;
+}
+
+/*
+ * Softmax attention for selected rows: rows[r] = h*N + n (rows == NULL: all H*N in order).
+ * q, k, v: BF16 bits [H][N][D]; out: FP64 [n_rows][D].  Scores, weights and sums in FP64,
+ * keys m ascending.
+ */
+int oracle_softmax_attention_rows(int64_t H, int64_t N, int64_t D, const uint16_t *q, const uint16_t *k,
+                                  const uint16_t *v, double scale, int64_t n_rows, const int64_t *rows, double *out)
+{
+    if (H < 0 || N < 1 || D < 1 || !q || !k || !v || !out || n_rows < 0)
+        return 1;
+    if (!rows && n_rows != H * N)
+        return 1;
+    int bad = 0;
+    int64_t r;
+#pragma omp parallel reduction(| : bad)
+    {
+        double *s = (double *)malloc((size_t)N * sizeof(double));
+        double *qd = (double *)malloc((size_t)D * sizeof(double));
+        if (!s || !qd)
+            bad |= 2;
+#pragma omp for schedule(dynamic, 4)
+        for (r = 0; r < n_rows; ++r) {
+            const int64_t flat = rows ? rows[r] : r;
+            if (!s || !qd || flat < 0 || flat >= H * N) {
+                bad |= 1;
+                continue;
+            }
+            const int64_t h = flat / N;
+            for (int64_t i = 0; i < D; ++i)
+                qd[i] = bf16_to_f64(q[flat * D + i]);
+            double smax = -INFINITY;
+            for (int64_t m = 0; m < N; ++m) {
+                const uint16_t *krow = k + (h * N + m) * D;
+                double dot = 0.0;
+                for (int64_t i = 0; i < D; ++i)
+                    dot += qd[i] * bf16_to_f64(krow[i]);
+                s[m] = scale * dot;
+                if (s[m] > smax)
+                    smax = s[m];
+            }
+            double wsum = 0.0;
+            for (int64_t m = 0; m < N; ++m) {
+                s[m] = exp(s[m] - smax);
+                wsum += s[m];
+            }
+            double *dst = out + r * D;
+            for (int64_t j = 0; j < D; ++j)
+                dst[j] = 0.0;
+            for (int64_t m = 0; m < N; ++m) {
+                const uint16_t *vrow = v + (h * N + m) * D;
+                for (int64_t j = 0; j < D; ++j)
+                    dst[j] += s[m] * bf16_to_f64(vrow[j]);
+            }
+            for (int64_t j = 0; j < D; ++j)
+                dst[j] /= wsum;
+        }
+        free(s);
+        free(qd);
     }
     return bad;
 }

@@ -56,6 +56,32 @@ def pins_hold(lib) -> bool:
     return True
 
 
+# Slips in the softmax anchor attention.
+SOFTMAX_MUTANTS = {
+    "no_max_subtraction": ("s[m] = exp(s[m] - smax);", "s[m] = exp(s[m]);"),
+    "no_scale": ("s[m] = scale * dot;", "s[m] = dot;"),
+    "no_normalisation": ("dst[j] /= wsum;", "dst[j] /= 1.0;"),
+    "value_of_wrong_key": ("const uint16_t *vrow = v + (h * N + m) * D;",
+                           "const uint16_t *vrow = v + (h * N + (N - 1 - m)) * D;"),
+    "keys_of_wrong_head": ("const uint16_t *krow = k + (h * N + m) * D;", "const uint16_t *krow = k + m * D;"),
+}
+
+
+def softmax_pins_hold(lib) -> bool:
+    from test_oracle_softmax_pins import bf16_randn, torch_sdpa
+    from conftest import to_bf16_bits, bits_to_f64
+    for shape, qs in (((2, 37, 16), 1.0), ((3, 64, 32), 3.0)):
+        qb, kb, vb = bf16_randn(shape, 1, qs), bf16_randn(shape, 2), bf16_randn(shape, 3)
+        got = oracle.softmax_attention_rows(qb, kb, vb, lib=lib).reshape(shape)
+        if not (np.all(np.isfinite(got)) and rel_l2(got, torch_sdpa(qb, kb, vb)) <= 1e-12):
+            return False
+    q = np.zeros((1, 6, 16)); q[..., 0] = 4096.0
+    k = np.zeros((1, 6, 16)); k[0, 3, 0] = 1.0
+    vb = bf16_randn((1, 6, 16), 9)
+    got = oracle.softmax_attention_rows(to_bf16_bits(q), to_bf16_bits(k), vb, lib=lib)
+    return bool(np.all(np.isfinite(got)) and np.allclose(got, bits_to_f64(vb)[0, 3], rtol=1e-12))
+
+
 def producer_pins_hold(lib) -> bool:
     from test_oracle_producer_pins import random_case, torch_producer
     for shape in ((2, 64, 32), (3, 17, 112)):
@@ -73,6 +99,17 @@ def producer_pins_hold(lib) -> bool:
 def test_unmodified_oracle_passes(oracle_lib):
     assert pins_hold(oracle_lib)
     assert producer_pins_hold(oracle_lib)
+    assert softmax_pins_hold(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(SOFTMAX_MUTANTS))
+def test_softmax_mutant_is_caught(tmp_path, name):
+    old, new = SOFTMAX_MUTANTS[name]
+    assert SRC.count(old) >= 1, f"mutation site for {name} not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(SRC.replace(old, new))
+    lib = oracle.load(lib_path=str(tmp_path / f"lib{name}.so"), src=str(src))
+    assert not softmax_pins_hold(lib), f"pins missed the planted slip {name}"
 
 
 @pytest.mark.parametrize("name", sorted(PRODUCER_MUTANTS))
