@@ -136,6 +136,20 @@ int lin_attn_forward_fused(lin_attn_ctx *ctx, const void *q, const void *k, cons
                            int64_t n_tokens, int mode, struct CUstream_st *stream);
 
 /*
+ * SANA-Video 2.0 softmax anchor layer (page "[sglang] SANA-Video 2.0 anchor attention의
+ * FP32 upcast 제거로 720p 생성 52% 단축하기", 코드 분석 §2: F.scaled_dot_product_attention(q,
+ * k, v, dropout_p=0.0) on BF16 [B, H, N, D], the page's 'high' path): per head,
+ *     out = softmax(scale * Q K^T) V         no mask; scale <= 0 means 1 / sqrt(head_dim)
+ *   q, k, v : BF16 [1, heads, n_tokens, head_dim] (the context's heads and head_dim)
+ *   out     : FP32 or BF16 [1, heads, n_tokens, head_dim]
+ * Flash-attention forward on tensor cores: FP32 scores and accumulator, the softmax
+ * weights rounded to BF16 for the second product.  Uses no scratch; timeouts are reported
+ * through lin_attn_device_status.
+ */
+int lin_attn_anchor_forward(lin_attn_ctx *ctx, const void *q, const void *k, const void *v, void *out,
+                            int out_dtype, int64_t n_tokens, float scale, struct CUstream_st *stream);
+
+/*
  * Same layer call on HOST buffers (same shapes and dtypes, any alignment).  Copies the
  * inputs to device staging owned by the context, runs the layer, copies the result
  * back and synchronises `stream` before returning: when it returns OK, `out` holds the

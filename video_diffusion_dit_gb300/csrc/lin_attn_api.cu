@@ -4,6 +4,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -397,6 +398,34 @@ int lin_attn_forward_fused(lin_attn_ctx* ctx, const void* q, const void* k, cons
     ctx->n_events = 0;
     return enqueue_heads(ctx, q, k, v, nullptr, out, out_dtype, n_tokens, mode, reinterpret_cast<cudaStream_t>(stream),
                          0, ctx->heads, ev, LIN_ATTN_LAYOUT_HND, rope_cos, rope_sin);
+}
+
+int lin_attn_anchor_forward(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, void* out,
+                            int out_dtype, int64_t n_tokens, float scale, struct CUstream_st* stream) {
+    if (!ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx is NULL");
+    if (!q || !k || !v || !out) return fail(LIN_ATTN_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (n_tokens < 1 || n_tokens > ctx->max_tokens)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "n_tokens=%lld outside [1, %lld]", (long long)n_tokens,
+                    (long long)ctx->max_tokens);
+    if (out_dtype != LIN_ATTN_OUT_F32 && out_dtype != LIN_ATTN_OUT_BF16)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "out_dtype=%d is not LIN_ATTN_OUT_F32/BF16", out_dtype);
+    if (!(scale >= 0.0f) || !(scale < 1e30f)) return fail(LIN_ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
+    DeviceScope scope(ctx->device);
+    if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    const int H = ctx->heads, D = ctx->head_dim;
+    const float s = scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+    const float log2e = 1.4426950408889634f;
+    CUtensorMap tq, tk, tv;
+    int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128);
+    if (rc) return rc;
+    if ((rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 64))) return rc;
+    if ((rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 64))) return rc;
+    cudaError_t e = la::launch_anchor_attention(tq, tk, tv, out, out_dtype == LIN_ATTN_OUT_BF16, H, n_tokens, D,
+                                                s * log2e, ctx->status, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "anchor_attention launch");
+    return ok();
 }
 
 int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,

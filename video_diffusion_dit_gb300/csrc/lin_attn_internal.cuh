@@ -206,4 +206,11 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
                             bool token_major, int grid, int* status, cudaStream_t stream,
                             const ProducerArgs* producer = nullptr);
 
+// Softmax anchor attention (flash forward): out = softmax(scale * Q K^T) V per head, no
+// mask.  Maps over [H][N][D] BF16: Q box (64, 128), K and V boxes (64, 64); scale_log2 =
+// scale * log2(e).
+cudaError_t launch_anchor_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                    void* out, bool out_bf16, int heads, int64_t n_tokens, int head_dim,
+                                    float scale_log2, int* status, cudaStream_t stream);
+
 }  // namespace la

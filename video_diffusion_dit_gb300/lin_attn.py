@@ -22,7 +22,7 @@ EXPORTS = (
     "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_layout", "lin_attn_forward_host",
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
-    "lin_attn_forward_noalloc", "lin_attn_forward_fused",
+    "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward",
 )
 
 
@@ -46,6 +46,7 @@ def _load():
         "lin_attn_version": ([], i32),
         "lin_attn_forward_noalloc": ([p, p, p, p, p, i32, i32, i64, i32, i32, p], i32),
         "lin_attn_forward_fused": ([p, p, p, p, p, p, p, i32, i64, i32, p], i32),
+        "lin_attn_anchor_forward": ([p, p, p, p, p, i32, i64, ctypes.c_float, p], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -210,6 +211,26 @@ class LinAttn:
                                         rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N, MODE_HIGH,
                                         _stream_handle(stream, self.device))
         _check(st, "lin_attn_forward_fused")
+        return out
+
+    def anchor_forward(self, q, k, v, out=None, out_dtype=torch.bfloat16, scale=None, stream=None):
+        """Softmax anchor attention (no mask, default scale 1/sqrt(D)) on [1, H, N, D] BF16."""
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"{name} must be a contiguous bfloat16 tensor on {self.device}")
+        if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.shape[0] != 1:
+            raise ValueError("q, k, v must share one [1, H, N, D] shape")
+        _, H, N, D = q.shape
+        if H != self.heads or D != self.head_dim:
+            raise ValueError(f"context is for H={self.heads}, D={self.head_dim}; got H={H}, D={D}")
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype, device=self.device)
+        elif out.shape != q.shape or not out.is_contiguous() or out.device != self.device:
+            raise ValueError("out must be a contiguous [1, H, N, D] tensor on the context's device")
+        st = lib.lin_attn_anchor_forward(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         _out_code(out.dtype), N, 0.0 if scale is None else float(scale),
+                                         _stream_handle(stream, self.device))
+        _check(st, "lin_attn_anchor_forward")
         return out
 
     def forward_host(self, q_rot, k_rot, v, normalizer, out=None, mode="high", out_dtype=torch.float32, stream=None):

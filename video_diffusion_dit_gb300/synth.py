@@ -145,5 +145,18 @@ def make_layer(heads: int, tokens: int, head_dim: int, seed: int = 0, grid=None,
     return out
 
 
+def make_anchor_layer(heads: int, tokens: int, head_dim: int, seed: int = 0, logit_scale: float = 1.0,
+                      device="cpu"):
+    """Inputs of a softmax anchor layer: q, k, v BF16 [1, H, N, D] ~ N(0, 1), q scaled by
+    `logit_scale` (spreads the attention logits)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    shape = (1, heads, tokens, head_dim)
+    q = (torch.randn(shape, generator=g, device=device) * logit_scale).to(torch.bfloat16)
+    k = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    return {"q": q, "k": k, "v": v}
+
+
 def make_workload(w: Workload, device="cpu", producer_inputs: bool = False):
     return make_layer(w.heads, w.tokens, w.head_dim, w.seed, w.grid, device, producer_inputs)
