@@ -4,12 +4,20 @@
 // 단축하기" (PR #49219), section 코드 분석, 2. GatedSoftmaxAttention: the anchor layer is
 // F.scaled_dot_product_attention(q, k, v, dropout_p=0.0) on BF16 [B, H, N, D] tensors (no
 // mask, default scale 1/sqrt(D)); the page's 'high' tier hands BF16 Q/K/V to a flash
-// kernel.  Here, per head and per 128-query tile:
-//     S = Q K^T (tcgen05, FP32 in TMEM), P = exp2(S * scale * log2 e - m) (BF16 in shared
-//     memory), O += P V (tcgen05, FP32 in TMEM), out = O / sum(P)
+// kernel.  Here, per head, for two 128-query tiles t = 0, 1 at once:
+//     S_t = Q_t K^T (tcgen05, FP32 in TMEM), P_t = exp2(S_t * scale * log2 e - m) (BF16,
+//     written back over the upper half of S_t in TMEM), O_t += P_t V (tcgen05 with A read
+//     from TMEM, FP32 in TMEM), out = O_t / sum(P_t)
 // with the running maximum m kept per row and O rescaled only when a row's maximum grows
 // by more than 8 (in log2 units) - the weights stay below 2^8, and O / sum(P) is exact for
 // any reference m - so the rescale (a TMEM read-modify-write) is rare.
+//
+// The two query tiles ping-pong: while one softmax warpgroup turns S_t(j) into weights, the
+// tensor pipe runs the other tile's products, in the issue order
+//     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
+// Tensor-core operations of one thread complete in issue order, so S_t(j) landing means
+// PV_t(j-1) has landed too: the softmax warps may rescale O_t right then, and S_t(j+1) may
+// overwrite the TMEM columns that PV_t(j) reads P_t(j) from.
 #include <cuda_bf16.h>
 
 #include "lin_attn_internal.cuh"
@@ -18,28 +26,69 @@
 namespace la {
 namespace {
 
-constexpr int kBM = 128;                  // query rows per CTA tile (MMA M, one row per thread)
-constexpr int kBN = 64;                   // keys per iteration
-constexpr int kAttnStages = 4;            // K/V ring
-constexpr int kAttnThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 softmax/epilogue
-constexpr uint32_t kQAtom = kBM * 128;    // 16 KB: 128 rows x 64 columns BF16 (128-byte swizzle)
-constexpr uint32_t kKVAtom = kBN * 128;   // 8 KB: 64 rows x 64 columns BF16
-constexpr uint32_t kPBytes = kBM * 128;   // 16 KB: P tile, 128 queries x 64 keys BF16
-constexpr float kRescaleSlack = 8.0f;     // rescale O when a row maximum grows by more than this
+constexpr int kBM = 128;                            // query rows per Q tile (MMA M, one row per thread)
+constexpr int kQTiles = 2;                          // Q tiles per CTA, one softmax warpgroup each
+constexpr int kBN = 128;                            // keys per K/V tile
+constexpr int kSlots = 5;                           // K/V ring: each slot holds one K or one V tile
+constexpr int kSoftmaxWarps = 4 * kQTiles;          // warps 0..7: softmax + epilogue
+constexpr int kMmaWarp = kSoftmaxWarps;             // warp 8: TMEM owner and MMA issuer
+constexpr int kTmaWarp = kSoftmaxWarps + 1;         // warp 9: TMA producer
+constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 2);
+constexpr uint32_t kAtom = 128 * 128;               // 16 KB: 128 rows x 64 BF16 columns, 128-byte swizzle
+constexpr float kRescaleSlack = 8.0f;               // rescale O when a row maximum grows by more than this
+// TMEM columns: S_t at 128 t, P_t over S_t's columns 64..127, O_t at 256 + 128 t.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;
+constexpr uint32_t kPCol = 64;
 
 template <int NBOX>
 struct AttnLayout {
-    static constexpr uint32_t q_bytes = NBOX * kQAtom;
-    static constexpr uint32_t stage_bytes = 2 * NBOX * kKVAtom;  // K tile + V tile
-    static constexpr uint32_t kv_offset = q_bytes;
-    static constexpr uint32_t p_offset = kv_offset + kAttnStages * stage_bytes;
-    static constexpr uint32_t bar_offset = p_offset + 2 * kPBytes;
+    static constexpr uint32_t tile_bytes = NBOX * kAtom;  // one Q, K or V tile
+    static constexpr uint32_t ring_offset = kQTiles * tile_bytes;
+    static constexpr uint32_t bar_offset = ring_offset + kSlots * tile_bytes;
     static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;
 };
 
-// TMEM columns: S buffers at 0 and 64, O at 128 (up to 128 columns).
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kOCol = 128;
+// Weights of 64 keys of one row, p = 2^(s * scale_log2 - m), written as packed BF16 pairs
+// (key 2c in the low half of column c) to the TMEM row at p_addr, 16 columns at a time;
+// returns the sum of the unrounded weights (four interleaved partial sums, added in a fixed
+// order).  The caller waits for the stores.
+__device__ __forceinline__ float half_weights(const uint32_t (&s)[64], float scale_log2, float neg_m,
+                                              uint32_t p_addr) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c = 16 * g + i;
+            const float x0 = __fmaf_rn(__uint_as_float(s[2 * c]), scale_log2, neg_m);
+            const float x1 = __fmaf_rn(__uint_as_float(s[2 * c + 1]), scale_log2, neg_m);
+            const float p0 = exp2_approx(x0), p1 = exp2_approx(x1);
+            acc[c & 3] += p0 + p1;
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&pp);
+        }
+        tmem_st16(p_addr + 16u * g, pk);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// Keys of a 64-column half past `valid` (relative to the half) become -inf.
+__device__ __forceinline__ void mask_half(uint32_t (&s)[64], int valid) {
+    if (valid < 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (c >= valid) s[c] = __float_as_uint(-INFINITY);
+    }
+}
+
+__device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(s[c]));
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
 
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -54,46 +103,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     const uint32_t bars = base + L::bar_offset;
     const uint32_t q_full = bars;
-    const uint32_t kv_full0 = bars + 8u;                         // [stages]
-    const uint32_t kv_empty0 = kv_full0 + 8u * kAttnStages;      // [stages]
-    const uint32_t s_full0 = kv_empty0 + 8u * kAttnStages;       // [2] S(j) in TMEM buffer j % 2
-    const uint32_t p_full0 = s_full0 + 16u;                      // [2] P(j) written (and S(j) read)
-    const uint32_t p_empty0 = p_full0 + 16u;                     // [2] PV(j) done reading P(j)
-    const uint32_t o_ready = p_empty0 + 16u;                     // one phase per PV
-    const uint32_t o_done = o_ready + 8u;                         // the last PV has landed
+    const uint32_t kv_full0 = bars + 8u;                      // [slots]
+    const uint32_t kv_empty0 = kv_full0 + 8u * kSlots;        // [slots]
+    const uint32_t s_full0 = kv_empty0 + 8u * kSlots;         // [tiles] S_t(j) in TMEM
+    const uint32_t p_full0 = s_full0 + 8u * kQTiles;          // [tiles] P_t(j) in TMEM, O_t rescaled
+    const uint32_t o_done = p_full0 + 8u * kQTiles;           // every product has landed
     const uint32_t drain_bar = o_done + 8u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 200);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int q_tiles = (n_tokens + kBM - 1) / kBM;
-    const int h = blockIdx.x / q_tiles;
-    const int m0 = (blockIdx.x % q_tiles) * kBM;
+    const int q_blocks = (n_tokens + kQTiles * kBM - 1) / (kQTiles * kBM);
+    const int h = blockIdx.x / q_blocks;
+    const int m0 = (blockIdx.x % q_blocks) * (kQTiles * kBM);
     const int n_kv = (n_tokens + kBN - 1) / kBN;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kAttnStages; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(kv_full0 + 8u * s, 1);
             mbar_init(kv_empty0 + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(s_full0 + 8u * b, 1);
-            mbar_init(p_full0 + 8u * b, 128);
-            mbar_init(p_empty0 + 8u * b, 1);
+        for (int t = 0; t < kQTiles; ++t) {
+            mbar_init(s_full0 + 8u * t, 1);
+            mbar_init(p_full0 + 8u * t, 4 * 32);
         }
-        mbar_init(o_ready, 1);
         mbar_init(o_done, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kTmaWarp && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -102,173 +147,160 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    auto slot_addr = [&](uint32_t i) { return base + L::ring_offset + (i % kSlots) * L::tile_bytes; };
 
-    if (warp == 0) {
+    if (warp == kTmaWarp) {
         if (lane == 0) {
-            // ---------------- producer: the Q tile once, then K/V tiles through the ring
+            // ---------------- producer: both Q tiles once, then K(0), V(0), K(1), V(1), ...
             const uint64_t pol_q = policy_evict_first();
-            mbar_arrive_expect_tx(q_full, NBOX * kQAtom);
+            mbar_arrive_expect_tx(q_full, kQTiles * L::tile_bytes);
 #pragma unroll
-            for (int x = 0; x < NBOX; ++x) tma_load_3d_hint(base + x * kQAtom, &tm_q, q_full, 64 * x, m0, h, pol_q);
+            for (int t = 0; t < kQTiles; ++t)
+#pragma unroll
+                for (int x = 0; x < NBOX; ++x)
+                    tma_load_3d_hint(base + t * L::tile_bytes + x * kAtom, &tm_q, q_full, 64 * x, m0 + kBM * t, h,
+                                     pol_q);
+            const uint32_t n_loads = 2u * static_cast<uint32_t>(n_kv);
+            uint32_t i = 0;
             bool ok = true;
-            uint32_t j = 0;
-            for (; j < static_cast<uint32_t>(n_kv); ++j) {
-                const uint32_t st = j % kAttnStages, ph = (j / kAttnStages) & 1u;
+            for (; i < n_loads; ++i) {
+                const uint32_t st = i % kSlots, ph = (i / kSlots) & 1u;
                 if (!mbar_wait(kv_empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t kt = base + L::kv_offset + st * L::stage_bytes;
-                const uint32_t vt = kt + NBOX * kKVAtom;
-                mbar_arrive_expect_tx(kv_full0 + 8u * st, L::stage_bytes);
+                mbar_arrive_expect_tx(kv_full0 + 8u * st, L::tile_bytes);
+                const CUtensorMap* map = (i & 1u) ? &tm_v : &tm_k;
+                const int key0 = static_cast<int>(i >> 1) * kBN;
 #pragma unroll
-                for (int x = 0; x < NBOX; ++x) {
-                    tma_load_3d(kt + x * kKVAtom, &tm_k, kv_full0 + 8u * st, 64 * x, j * kBN, h);
-                    tma_load_3d(vt + x * kKVAtom, &tm_v, kv_full0 + 8u * st, 64 * x, j * kBN, h);
-                }
+                for (int x = 0; x < NBOX; ++x)
+                    tma_load_3d(slot_addr(i) + x * kAtom, map, kv_full0 + 8u * st, 64 * x, key0, h);
             }
-            if (!ok) {
-                const uint32_t first = j > kAttnStages ? j - kAttnStages : 0;
-                for (uint32_t i = first; i < j; ++i)
-                    mbar_wait_drain(kv_full0 + 8u * (i % kAttnStages), (i / kAttnStages) & 1u);
+            if (!ok) {  // let the copies in flight land before the CTA exits
+                const uint32_t first = i > kSlots ? i - kSlots : 0;
+                for (uint32_t k = first; k < i; ++k) mbar_wait_drain(kv_full0 + 8u * (k % kSlots), (k / kSlots) & 1u);
                 mbar_wait_drain(q_full, 0);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            // ---------------- MMA issuer: S(0), S(1), then per tile j: PV(j), S(j + 2)
+            // ---------------- MMA issuer
             const uint32_t idesc_s = make_idesc_bf16_f32(kBM, kBN, false, false);      // Q, K both K-major
-            const uint32_t idesc_o = make_idesc_bf16_f32(kBM, head_dim, false, true);  // P K-major, V MN-major
-            const uint32_t qa = base;
-            auto issue_s = [&](uint32_t jj) -> bool {
-                const uint32_t st = jj % kAttnStages, ph = (jj / kAttnStages) & 1u;
-                if (!mbar_wait(kv_full0 + 8u * st, ph, abort_flag, status)) return false;
-                tc_fence_after();
-                const uint32_t kt = base + L::kv_offset + st * L::stage_bytes;
-                const uint32_t d = tmem + (jj & 1u) * kBN;
-#pragma unroll
-                for (int ks = 0; ks < 4 * NBOX; ++ks) {
-                    const uint32_t x = ks >> 2, off = (ks & 3) * 32u;
-                    const uint64_t ad = make_smem_desc(qa + x * kQAtom + off, 16u, 1024u, kSwizzle128B);
-                    const uint64_t bd = make_smem_desc(kt + x * kKVAtom + off, 16u, 1024u, kSwizzle128B);
-                    mma_bf16(d, ad, bd, idesc_s, ks != 0 ? 1u : 0u);
-                }
-                mma_commit(s_full0 + 8u * (jj & 1u));
-                return true;
+            const uint32_t idesc_o = make_idesc_bf16_f32(kBM, head_dim, false, true);  // P K-major (TMEM), V MN-major
+            const int ksteps = head_dim / 16;
+            auto wait_full = [&](uint32_t i) {
+                return mbar_wait(kv_full0 + 8u * (i % kSlots), (i / kSlots) & 1u, abort_flag, status);
             };
-            bool ok = mbar_wait(q_full, 0, abort_flag, status);
-            if (ok) tc_fence_after();
-            for (uint32_t jj = 0; ok && jj < 2 && jj < static_cast<uint32_t>(n_kv); ++jj) ok = issue_s(jj);
-            for (uint32_t j = 0; ok && j < static_cast<uint32_t>(n_kv); ++j) {
-                const uint32_t b = j & 1u;
-                if (!mbar_wait(p_full0 + 8u * b, (j >> 1) & 1u, abort_flag, status)) break;
-                tc_fence_after();
-                const uint32_t st = j % kAttnStages;
-                const uint32_t vt = base + L::kv_offset + st * L::stage_bytes + NBOX * kKVAtom;
-                const uint32_t pa = base + L::p_offset + b * kPBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t ad = make_smem_desc(pa + kk * 32u, 16u, 1024u, kSwizzle128B);
-                    const uint64_t bd = make_smem_desc(vt + kk * 2048u, kKVAtom, 1024u, kSwizzle128B);
-                    mma_bf16(tmem + kOCol, ad, bd, idesc_o, (j | kk) != 0 ? 1u : 0u);
+            auto issue_s = [&](int t, uint32_t kslot) {
+                const uint32_t qa = base + t * L::tile_bytes;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint32_t off = (ks >> 2) * kAtom + (ks & 3) * 32u;
+                    mma_bf16(tmem + 128u * t, make_smem_desc(qa + off, 16u, 1024u, kSwizzle128B),
+                             make_smem_desc(kslot + off, 16u, 1024u, kSwizzle128B), idesc_s, ks != 0 ? 1u : 0u);
                 }
-                mma_commit(p_empty0 + 8u * b);
-                mma_commit(kv_empty0 + 8u * st);
-                mma_commit(o_ready);
-                if (j + 1 == static_cast<uint32_t>(n_kv)) mma_commit(o_done);
-                if (j + 2 < static_cast<uint32_t>(n_kv)) ok = issue_s(j + 2);
+                mma_commit(s_full0 + 8u * t);
+            };
+            auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_bf16_ts(tmem + kOCol + 128u * t, tmem + 128u * t + kPCol + 8u * kk,
+                                make_smem_desc(vslot + kk * 2048u, kAtom, 1024u, kSwizzle128B), idesc_o,
+                                (accumulate || kk != 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(q_full, 0, abort_flag, status) && wait_full(0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, slot_addr(0));
+                issue_s(1, slot_addr(0));
+                mma_commit(kv_empty0 + 8u * (0 % kSlots));
             }
+            for (uint32_t j = 0; ok && j < static_cast<uint32_t>(n_kv); ++j) {
+                const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
+                const bool more = j + 1 < static_cast<uint32_t>(n_kv);
+                if (!(ok = wait_full(iv) && mbar_wait(p_full0, j & 1u, abort_flag, status))) break;
+                tc_fence_after();
+                issue_pv(0, slot_addr(iv), j > 0);
+                if (more) {
+                    if (!(ok = wait_full(ik))) break;
+                    tc_fence_after();
+                    issue_s(0, slot_addr(ik));
+                }
+                if (!(ok = mbar_wait(p_full0 + 8u, j & 1u, abort_flag, status))) break;
+                tc_fence_after();
+                issue_pv(1, slot_addr(iv), j > 0);
+                mma_commit(kv_empty0 + 8u * (iv % kSlots));
+                if (more) {
+                    issue_s(1, slot_addr(ik));
+                    mma_commit(kv_empty0 + 8u * (ik % kSlots));
+                }
+            }
+            if (ok) mma_commit(o_done);
             mma_commit(drain_bar);
             mbar_wait_drain(drain_bar, 0);
         }
     } else {
-        // ---------------- softmax and epilogue: thread = query row r of the tile
+        // ---------------- softmax and epilogue: warpgroup t, thread = query row r of Q tile t
+        const int t = warp >> 2;
         const int q = warp & 3;
         const int r = 32 * q + lane;
-        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t s_addr = tmem + lane_base + 128u * t;
+        const uint32_t o_addr = tmem + lane_base + kOCol + 128u * t;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const uint32_t b = j & 1u;
-            if (!mbar_wait(s_full0 + 8u * b, (j >> 1) & 1u, abort_flag, status)) {
-                ok = false;
-                break;
-            }
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = mbar_wait(s_full0 + 8u * t, j & 1u, abort_flag, status))) break;
             tc_fence_after();
-            uint32_t sraw[2][32];
-            tmem_ld32_sync(tmem + lane_addr + b * kBN, sraw[0]);
-            tmem_ld32_sync(tmem + lane_addr + b * kBN + 32, sraw[1]);
-            float t[kBN];
-            float tmax = -INFINITY;
+            // Row maximum over both 64-key halves; keep the upper half in registers.
             const int valid = min(kBN, n_tokens - j * kBN);  // keys past the end are masked out
+            uint32_t s[64];
+            tmem_ld64_sync(s_addr, s);
+            mask_half(s, valid);
+            const float mx_lo = half_max(s);
+            tmem_ld64_sync(s_addr + 64u, s);
+            mask_half(s, valid - 64);
+            const float m_tile = fmaxf(mx_lo, half_max(s)) * scale_log2;
+            if (j == 0) {
+                m_ref = m_tile;
+            } else {
+                // Lazy rescale, warp by warp (a warp reaches only its own 32 TMEM lanes).  O_t
+                // holds exactly PV_t(0 .. j-1) here: S_t(j) was issued after PV_t(j-1), and
+                // PV_t(j) waits for this warpgroup's arrival below.
+                const bool grow = m_tile > m_ref + kRescaleSlack;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = grow ? exp2_approx(m_ref - m_tile) : 1.0f;
+                    for (int c = 0; c < head_dim; c += 16) {
+                        uint32_t o[16];
+                        tmem_ld16_sync(o_addr + c, o);
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                t[c] = c < valid ? __uint_as_float(sraw[c >> 5][c & 31]) * scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, t[c]);
-            }
-            // Lazy rescale: the whole warp rescales together (TMEM access is warp-wide).
-            const bool grow = j > 0 && tmax > m_ref + kRescaleSlack;
-            if (__any_sync(0xffffffffu, grow)) {
-                // O must hold PV(j - 1) before it is rescaled.  S(j) was issued after
-                // PV(j - 2) and has landed, so PV(j - 2) is done and the PV count is j - 1 or
-                // j: o_ready's parity tells the two apart.
-                if (!mbar_wait(o_ready, (j - 1) & 1u, abort_flag, status)) {
-                    ok = false;
-                    break;
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st16(o_addr + c, o);
+                    }
+                    if (grow) {
+                        l *= alpha;
+                        m_ref = m_tile;
+                    }
                 }
-                tc_fence_after();
-                const float alpha = grow ? exp2_approx(m_ref - tmax) : 1.0f;
-                for (int c = 0; c < head_dim; c += 16) {
-                    uint32_t o[16];
-                    tmem_ld16_sync(tmem + lane_addr + kOCol + c, o);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st16(tmem + lane_addr + kOCol + c, o);
-                }
-                tmem_st_wait();
-                if (grow) {
-                    l *= alpha;
-                    m_ref = tmax;
-                }
             }
-            if (j == 0) m_ref = tmax;
-            // Weights, their running sum, and the BF16 P row for the next MMA.
-            uint32_t pw[kBN / 2];
-#pragma unroll
-            for (int c = 0; c < kBN; c += 2) {
-                const float p0 = exp2_approx(t[c] - m_ref);
-                const float p1 = exp2_approx(t[c + 1] - m_ref);
-                l += p0;
-                l += p1;
-                const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-                pw[c / 2] = *reinterpret_cast<const uint32_t*>(&pp);
-            }
-            // P buffer b is free once PV(j - 2) has read it.
-            if (!mbar_wait(p_empty0 + 8u * b, ((j >> 1) & 1u) ^ 1u, abort_flag, status)) {
-                ok = false;
-                break;
-            }
-            const uint32_t prow = base + L::p_offset + b * kPBytes + r * 128u;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t addr = prow + ((static_cast<uint32_t>(c) ^ (r & 7u)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pw[4 * c]),
-                             "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
-                             : "memory");
-            }
-            fence_proxy_async_smem();
+            // P_t(j) over S_t(j)'s columns 64..127: first the weights of keys 64..127 (their
+            // P columns 96..127 hold S values already in registers), then keys 0..63 from a
+            // second load of S columns 0..63 (their P columns 64..95 are consumed S too).
+            l += half_weights(s, scale_log2, -m_ref, s_addr + kPCol + 32u);
+            tmem_ld64_sync(s_addr, s);
+            mask_half(s, valid);
+            l += half_weights(s, scale_log2, -m_ref, s_addr + kPCol);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(p_full0 + 8u * b);
+            mbar_arrive(p_full0 + 8u * t);
         }
-        // Epilogue: O / l once the last PV has landed (a barrier of its own: by now the PV
-        // count can be one of three values, too many for o_ready's parity).
+        // Epilogue: O_t / l once the last product has landed.
         if (ok && mbar_wait(o_done, 0, abort_flag, status)) {
             tc_fence_after();
-            const int row = m0 + r;
+            const int row = m0 + kBM * t + r;
             const float inv = 1.0f / l;
             for (int c = 0; c < head_dim; c += 16) {
                 uint32_t o[16];
-                tmem_ld16_sync(tmem + lane_addr + kOCol + c, o);
+                tmem_ld16_sync(o_addr + c, o);
                 if (row < n_tokens) {
                     const int64_t off = (static_cast<int64_t>(h) * n_tokens + row) * head_dim + c;
                     if (OUT_BF16) {
@@ -297,7 +329,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -310,8 +342,8 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     cudaError_t e = cudaFuncSetAttribute(anchor_attention_kernel<NBOX, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
     if (e != cudaSuccess) return e;
-    const int q_tiles = (n_tokens + kBM - 1) / kBM;
-    anchor_attention_kernel<NBOX, BF16><<<heads * q_tiles, kAttnThreads, L::smem_bytes, stream>>>(
+    const int q_blocks = (n_tokens + kQTiles * kBM - 1) / (kQTiles * kBM);
+    anchor_attention_kernel<NBOX, BF16><<<heads * q_blocks, kAttnThreads, L::smem_bytes, stream>>>(
         tq, tk, tv, out, n_tokens, head_dim, scale_log2, status);
     return cudaGetLastError();
 }

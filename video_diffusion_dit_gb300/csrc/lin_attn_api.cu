@@ -420,8 +420,8 @@ int lin_attn_anchor_forward(lin_attn_ctx* ctx, const void* q, const void* k, con
     CUtensorMap tq, tk, tv;
     int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128);
     if (rc) return rc;
-    if ((rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 64))) return rc;
-    if ((rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 64))) return rc;
+    if ((rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128))) return rc;
+    if ((rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128))) return rc;
     cudaError_t e = la::launch_anchor_attention(tq, tk, tv, out, out_dtype == LIN_ATTN_OUT_BF16, H, n_tokens, D,
                                                 s * log2e, ctx->status, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "anchor_attention launch");
