@@ -51,27 +51,32 @@ struct AttnLayout {
 
 // Weights of 64 keys of one row, p = 2^(s * scale_log2 - m), written as packed BF16 pairs
 // (key 2c in the low half of column c) to the TMEM row at p_addr, 16 columns at a time;
-// returns the sum of the unrounded weights (four interleaved partial sums, added in a fixed
+// returns the sum of the unrounded weights (two paired partial sums, added in a fixed
 // order).  The caller waits for the stores.
-__device__ __forceinline__ float half_weights(const uint32_t (&s)[64], float scale_log2, float neg_m,
+__device__ __forceinline__ float half_weights(const uint32_t (&s)[64], uint64_t scale2, uint64_t neg_m2,
                                               uint32_t p_addr) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int c = 16 * g + i;
-            const float x0 = __fmaf_rn(__uint_as_float(s[2 * c]), scale_log2, neg_m);
-            const float x1 = __fmaf_rn(__uint_as_float(s[2 * c + 1]), scale_log2, neg_m);
+            float x0, x1;
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), scale2,
+                                   neg_m2),
+                         x0, x1);
             const float p0 = exp2_approx(x0), p1 = exp2_approx(x1);
-            acc[c & 3] += p0 + p1;
+            acc[c & 1] = f32x2_add(acc[c & 1], f32x2_pack(p0, p1));
             const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
             pk[i] = *reinterpret_cast<const uint32_t*>(&pp);
         }
         tmem_st16(p_addr + 16u * g, pk);
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    float a0, a1, b0, b1;
+    f32x2_unpack(acc[0], a0, a1);
+    f32x2_unpack(acc[1], b0, b1);
+    return (a0 + a1) + (b0 + b1);
 }
 
 // Keys of a 64-column half past `valid` (relative to the half) become -inf.
@@ -86,7 +91,8 @@ __device__ __forceinline__ void mask_half(uint32_t (&s)[64], int valid) {
 __device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(s[c]));
+    for (int c = 0; c < 64; c += 2)
+        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
     return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
 }
 
@@ -285,10 +291,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // P_t(j) over S_t(j)'s columns 64..127: first the weights of keys 64..127 (their
             // P columns 96..127 hold S values already in registers), then keys 0..63 from a
             // second load of S columns 0..63 (their P columns 64..95 are consumed S too).
-            l += half_weights(s, scale_log2, -m_ref, s_addr + kPCol + 32u);
+            const uint64_t scale2 = f32x2_pack(scale_log2, scale_log2), neg_m2 = f32x2_pack(-m_ref, -m_ref);
+            l += half_weights(s, scale2, neg_m2, s_addr + kPCol + 32u);
             tmem_ld64_sync(s_addr, s);
             mask_half(s, valid);
-            l += half_weights(s, scale_log2, -m_ref, s_addr + kPCol);
+            l += half_weights(s, scale2, neg_m2, s_addr + kPCol);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full0 + 8u * t);
