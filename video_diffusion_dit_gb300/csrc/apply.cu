@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
         const bool live = 8 * c < head_dim;
         const int64_t pairs = head_dim / 2;
         const uint64_t tpol = policy_evict_last();
-        float ks[8];
+        uint64_t ks[4];  // the head's column sums in rope_chunk's activation order
         int cur_h = -1;
         uint32_t it = 0;
         for (int t = t_begin; t < t_end; ++t, ++it) {
@@ -234,8 +234,12 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
             if (h != cur_h) {
                 if (cur_h < 0) grid_dependency_wait();  // the column sums come from the reduction
                 cur_h = h;
+                const float* kh = pa.ksum + h * head_dim + 8 * c;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ks[e] = live ? pa.ksum[h * head_dim + 8 * c + e] : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int col = e < 2 ? 4 * e : 4 * (e - 2) + 1;
+                    ks[e] = live ? f32x2_pack(kh[col], kh[col + 2]) : 0ull;
+                }
             }
             const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
             const uint32_t buf = lt & 1u;
@@ -250,10 +254,15 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
                 if (live && n < n_tokens) {
                     uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                     uint4 w = *cell;
-                    float act[8];
-                    rope_chunk(w, cv[k], sv[k], act);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) part = __fmaf_rn(act[e], ks[e], part);
+                    uint64_t a0[2], a1[2];
+                    rope_chunk(w, cv[k], sv[k], a0, a1);
+                    uint64_t d2 = f32x2_mul(a0[0], ks[0]);
+                    d2 = f32x2_fma(a0[1], ks[1], d2);
+                    d2 = f32x2_fma(a1[0], ks[2], d2);
+                    d2 = f32x2_fma(a1[1], ks[3], d2);
+                    float d0, d1;
+                    f32x2_unpack(d2, d0, d1);
+                    part = d0 + d1;
                     *cell = w;
                 }
                 part += __shfl_xor_sync(0xffffffffu, part, 8);

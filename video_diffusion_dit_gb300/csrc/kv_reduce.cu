@@ -230,11 +230,13 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
             const int h = static_cast<int>(t / tph);
             const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
-            // Column sums of relu(K), compensated binary32 summation (sum + running error
-            // term, fixed order): FP64-class accuracy at FP32 rate.
-            float ks[8], kc[8];
+            // Column sums of relu(K): each tile's 8 rows in plain binary32 pairs, folded into a
+            // compensated binary32 running sum (sum + running error term) once per tile, in a
+            // fixed order: FP64-class accuracy at FP32 rate.  Pair e holds columns
+            // {4e, 4e + 2} (e < 2) or {4(e-2) + 1, 4(e-2) + 3} of the thread's chunk.
+            uint64_t ks[4], kc[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ks[e] = kc[e] = 0.f;
+            for (int e = 0; e < 4; ++e) ks[e] = kc[e] = 0ull;
             for (; t < seg_end; ++t, ++it) {
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
                 if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status)) {
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     uint8_t* stage = base_ptr + st * L::stage_bytes;
                     uint8_t* atom = stage + (c >> 3) * kKvAtomBytes;
                     const uint8_t* tab = stage + L::a_bytes + L::b_bytes + 16 * c;  // [64][pairs] floats
+                    uint64_t ts[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int k8 = 0; k8 < kKvTile / 8; ++k8) {
                         const int r = rg + 8 * k8;
@@ -254,17 +257,21 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                             uint4 w = *cell;
                             const float4 c4 = *reinterpret_cast<const float4*>(tab + r * pairs * 4);
                             const float4 s4 = *reinterpret_cast<const float4*>(tab + L::tab_bytes + r * pairs * 4);
-                            float act[8];
-                            rope_chunk(w, c4, s4, act);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float yv = __fsub_rn(act[e], kc[e]);
-                                const float tsum = __fadd_rn(ks[e], yv);
-                                kc[e] = __fsub_rn(__fsub_rn(tsum, ks[e]), yv);
-                                ks[e] = tsum;
-                            }
+                            uint64_t a0[2], a1[2];
+                            rope_chunk(w, c4, s4, a0, a1);
+                            ts[0] = f32x2_add(ts[0], a0[0]);
+                            ts[1] = f32x2_add(ts[1], a0[1]);
+                            ts[2] = f32x2_add(ts[2], a1[0]);
+                            ts[3] = f32x2_add(ts[3], a1[1]);
                             *cell = w;
                         }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint64_t yv = f32x2_sub(ts[e], kc[e]);
+                        const uint64_t tsum = f32x2_add(ks[e], yv);
+                        kc[e] = f32x2_sub(f32x2_sub(tsum, ks[e]), yv);
+                        ks[e] = tsum;
                     }
                 }
                 fence_proxy_async_smem();
@@ -277,7 +284,14 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                 const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
                 double* dst = pa.ksum_partial + (slot * 8 + rg) * head_dim + 8 * c;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dst[e] = static_cast<double>(ks[e]) - static_cast<double>(kc[e]);
+                for (int e = 0; e < 4; ++e) {
+                    float s0, s1, c0, c1;
+                    f32x2_unpack(ks[e], s0, s1);
+                    f32x2_unpack(kc[e], c0, c1);
+                    const int col = e < 2 ? 4 * e : 4 * (e - 2) + 1;
+                    dst[col] = static_cast<double>(s0) - static_cast<double>(c0);
+                    dst[col + 2] = static_cast<double>(s1) - static_cast<double>(c1);
+                }
             }
         }
     } else if (!FUSED || warp < 6) {

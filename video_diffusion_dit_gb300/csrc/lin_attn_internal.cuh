@@ -139,24 +139,32 @@ constexpr float kDenEps = 1e-6f;
 
 // Producer step on one 16-byte chunk (8 BF16 values = 4 rotation pairs) of a Q or K row:
 // ReLU, then each pair (x0, x1) is turned by (c, s) as (x0 c - x1 s, x0 s + x1 c) with
-// binary32 products and sums in exactly this order (no fused multiply-add), rounded once to
-// BF16 (nearest-even).  The activated (un-rotated) values are returned in `act` for the
-// normaliser.
-__device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const float4 s4, float (&act)[8]) {
+// binary32 products and sums in exactly this order, rounded once to BF16 (nearest-even).
+// The rotation stays on scalar round-to-nearest intrinsics, which the compiler never fuses
+// into a multiply-add (a paired multiply feeding a paired add can be fused, which moves
+// exact ties).  The activated (un-rotated) values come back for the normaliser as paired
+// registers act0[h] = {x0 of pairs 2h, 2h + 1} (chunk columns 4h, 4h + 2) and
+// act1[h] = {x1 of the same pairs} (columns 4h + 1, 4h + 3).
+__device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const float4 s4, uint64_t (&act0)[2],
+                                           uint64_t (&act1)[2]) {
     const uint32_t in[4] = {w.x, w.y, w.z, w.w};
     uint32_t outw[4];
+    float x0[4], x1[4];
     const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
     const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float x0 = fmaxf(__uint_as_float(in[j] << 16), 0.f);
-        const float x1 = fmaxf(__uint_as_float(in[j] & 0xFFFF0000u), 0.f);
-        act[2 * j] = x0;
-        act[2 * j + 1] = x1;
-        const float y0 = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
-        const float y1 = __fadd_rn(__fmul_rn(x0, sn[j]), __fmul_rn(x1, cs[j]));
+        x0[j] = fmaxf(__uint_as_float(in[j] << 16), 0.f);
+        x1[j] = fmaxf(__uint_as_float(in[j] & 0xFFFF0000u), 0.f);
+        const float y0 = __fsub_rn(__fmul_rn(x0[j], cs[j]), __fmul_rn(x1[j], sn[j]));
+        const float y1 = __fadd_rn(__fmul_rn(x0[j], sn[j]), __fmul_rn(x1[j], cs[j]));
         const __nv_bfloat162 y = __floats2bfloat162_rn(y0, y1);
         outw[j] = *reinterpret_cast<const uint32_t*>(&y);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        act0[h] = f32x2_pack(x0[2 * h], x0[2 * h + 1]);
+        act1[h] = f32x2_pack(x1[2 * h], x1[2 * h + 1]);
     }
     w = make_uint4(outw[0], outw[1], outw[2], outw[3]);
 }
