@@ -24,18 +24,48 @@ namespace {
 // the reciprocal denominator and write 32-row boxes through swizzled staging with TMA
 // stores.  BF16 x BF16 products are exact in FP32 and the three terms carry 24 bits of
 // KV, so the result has FP32-class accuracy (the tier's second GEMM "stays FP32").
-constexpr int kApplyStages = 3;
+constexpr int kApplyStagesPlain = 3;
+// The fused path spends shared memory on rotation-table rows instead: fewer Q stages and
+// epilogue staging buffers.
+#ifndef LA_FUSED_Q_STAGES
+#define LA_FUSED_Q_STAGES 2
+#endif
+#ifndef LA_FUSED_OUT_BUFS
+#define LA_FUSED_OUT_BUFS 1
+#endif
+#ifndef LA_FUSED_TAB_ROWS_MAX
+#define LA_FUSED_TAB_ROWS_MAX 64
+#endif
+constexpr int kApplyStagesFused = LA_FUSED_Q_STAGES;
+constexpr int kOutBufsFused = LA_FUSED_OUT_BUFS;
 constexpr int kApplyThreads = 192;
 constexpr int kApplyThreadsFused = 448;  // + warps 6..13: the producer-step transform
 constexpr int kApplyTransformThreads = 256;
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
 constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
 
-__host__ __device__ inline uint32_t apply_smem_bytes(int head_dim, bool fused) {
+// Fused path: a ring of two slots, each holding the rotation-table rows (cos, then sin) of
+// tab_rows consecutive tokens: half a tile where that fits in shared memory, else a quarter.
+constexpr uint32_t kSmemLimit = 232448;
+
+__host__ __device__ constexpr uint32_t apply_smem_bytes_with(int head_dim, bool fused, int tab_rows) {
     const uint32_t nbox = head_dim_atoms(head_dim);
-    return static_cast<uint32_t>(kv_image_bytes(head_dim)) + kApplyStages * nbox * kQAtomBytes +
-           4 * 2 * kOutBoxBytes + 256 + (fused ? 2 * kApplyTile * 4 : 0) + 1024;
+    return static_cast<uint32_t>(kv_image_bytes(head_dim)) +
+           (fused ? kApplyStagesFused : kApplyStagesPlain) * nbox * kQAtomBytes +
+           4 * (fused ? kOutBufsFused : 2) * kOutBoxBytes +
+           (fused ? 2u * tab_rows * (head_dim / 2) * 4u * 2u : 0u) + 256 + (fused ? 2 * kApplyTile * 4 : 0) + 1024;
 }
+__host__ __device__ constexpr int apply_tab_rows(int head_dim) {
+    return apply_smem_bytes_with(head_dim, true, LA_FUSED_TAB_ROWS_MAX) <= kSmemLimit ? LA_FUSED_TAB_ROWS_MAX
+                                                                                       : LA_FUSED_TAB_ROWS_MAX / 2;
+}
+__host__ __device__ constexpr uint32_t apply_smem_bytes(int head_dim, bool fused) {
+    return apply_smem_bytes_with(head_dim, fused, fused ? apply_tab_rows(head_dim) : 0);
+}
+// The largest head dim must fit, with whole 16-row groups of table rows per slot.
+static_assert(apply_smem_bytes(128, true) <= kSmemLimit && apply_smem_bytes(128, false) <= kSmemLimit,
+              "apply layout exceeds shared memory");
+static_assert(apply_tab_rows(128) >= 16 && apply_tab_rows(16) % 16 == 0, "table slots must hold 16-row groups");
 
 template <int NBOX, bool OUT_BF16, bool FUSED>
 __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
@@ -47,12 +77,18 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
 
+    constexpr int kApplyStages = FUSED ? kApplyStagesFused : kApplyStagesPlain;
+    constexpr uint32_t kOutBufs = FUSED ? kOutBufsFused : 2u;  // staging buffers per epilogue warp
     const uint32_t img_bytes = 3u * NBOX * head_dim * 128u;
     const uint32_t term_bytes = NBOX * head_dim * 128u;
+    const int tab_rows = FUSED ? apply_tab_rows(head_dim) : kApplyTile;  // tokens per table slot
+    const uint32_t tab_subs = kApplyTile / tab_rows;                     // table slots per tile
+    const uint32_t tab_slot = FUSED ? static_cast<uint32_t>(tab_rows) * (head_dim / 2) * 4u * 2u : 0u;
     const uint32_t b_smem = base;
     const uint32_t q_smem = b_smem + img_bytes;
     const uint32_t o_smem = q_smem + kApplyStages * NBOX * kQAtomBytes;
-    const uint32_t bar_off = img_bytes + kApplyStages * NBOX * kQAtomBytes + 8 * kOutBoxBytes;
+    const uint32_t tab_smem = o_smem + 4 * kOutBufs * kOutBoxBytes;
+    const uint32_t bar_off = tab_smem + 2 * tab_slot - base;
     const uint32_t bars = base + bar_off;
     const uint32_t q_full0 = bars;                        // [kApplyStages]
     const uint32_t q_empty0 = bars + 8u * kApplyStages;   // [kApplyStages]
@@ -64,6 +100,8 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     const uint32_t q_ready0 = drain_bar + 8u;             // [kApplyStages] (fused: tile transformed)
     const uint32_t den_full0 = q_ready0 + 8u * kApplyStages;  // [2] (fused: row denominators written)
     const uint32_t den_empty0 = den_full0 + 16u;          // [2] (fused: row denominators read)
+    const uint32_t tab_full0 = den_empty0 + 16u;          // [2] (fused: half-tile table rows landed)
+    const uint32_t tab_empty0 = tab_full0 + 16u;          // [2] (fused: half-tile table rows used)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + 200);
     float* den_s = reinterpret_cast<float*>(base_ptr + bar_off + 256);  // fused: [2][kApplyTile]
@@ -85,6 +123,8 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
             if (FUSED) {
                 mbar_init(den_full0 + 8u * b, kApplyTransformThreads);
                 mbar_init(den_empty0 + 8u * b, 4);
+                mbar_init(tab_full0 + 8u * b, 1);
+                mbar_init(tab_empty0 + 8u * b, kApplyTransformThreads);
             }
             mbar_init(acc_full0 + 8u * b, 1);
             mbar_init(acc_empty0 + 8u * b, 4);
@@ -121,6 +161,7 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             bool ok = true, b_pending = false;
+            uint32_t tab_issued = 0;  // half-tile table loads issued
             for (int t = t_begin; t < t_end; ++t, ++it) {
                 const int h = t / tiles_per_head;
                 const int n0 = (t % tiles_per_head) * kApplyTile;
@@ -150,12 +191,45 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
                     bulk_load(b_smem, kv_image + static_cast<int64_t>(h) * img_bytes, img_bytes, b_full);
                     b_pending = true;
                 }
+                if (FUSED) {
+                    // The tile's rotation-table rows, tab_rows tokens per slot: rows are
+                    // contiguous in the [N][D/2] tables, so a slot is one bulk copy per table,
+                    // cut at N.
+                    const uint32_t row_bytes = static_cast<uint32_t>(head_dim / 2) * 4u;
+                    for (uint32_t hh = 0; hh < tab_subs && ok; ++hh) {
+                        const uint32_t i = tab_subs * it + hh;
+                        const uint32_t slot = i & 1u, tph = (i >> 1) & 1u;
+                        if (!mbar_wait(tab_empty0 + 8u * slot, tph ^ 1u, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        const int r0 = n0 + static_cast<int>(hh) * tab_rows;
+                        const int rows = max(0, min(tab_rows, n_tokens - r0));
+                        const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
+                        const uint32_t dst = tab_smem + slot * tab_slot;
+                        mbar_arrive_expect_tx(tab_full0 + 8u * slot, 2u * bytes);
+                        if (rows > 0) {
+                            bulk_load(dst, pa.cos + static_cast<int64_t>(r0) * (head_dim / 2), bytes, tab_full0 + 8u * slot);
+                            bulk_load(dst + tab_slot / 2, pa.sin + static_cast<int64_t>(r0) * (head_dim / 2), bytes,
+                                      tab_full0 + 8u * slot);
+                        }
+                        tab_issued = i + 1;
+                    }
+                    if (!ok) {
+                        ++it;
+                        break;
+                    }
+                }
             }
             if (!ok) {
                 const uint32_t first = it > kApplyStages ? it - kApplyStages : 0;
                 for (uint32_t j = first; j < it; ++j)
                     mbar_wait_drain(q_full0 + 8u * (j % kApplyStages), (j / kApplyStages) & 1u);
                 if (b_pending) mbar_wait_drain(b_full, run & 1);
+                if (FUSED) {
+                    const uint32_t tfirst = tab_issued > 2u ? tab_issued - 2u : 0u;  // two slots
+                    for (uint32_t j = tfirst; j < tab_issued; ++j) mbar_wait_drain(tab_full0 + 8u * (j & 1u), (j >> 1) & 1u);
+                }
             }
         }
     } else if (warp == 1) {
@@ -206,12 +280,11 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
         // ReLU, dot with the head's column sums of relu(K) (the normaliser), then the rotation
         // (binary32 products and sum in a fixed order, rounded once to BF16).  The 16 threads of
         // a row add their dot products in a fixed butterfly; the row's denominator goes to
-        // den_s for the epilogue.  The tile's table rows are requested before its wait.
+        // den_s for the epilogue.  Table rows come from the half-tile slots the producer fills.
         const int u = threadIdx.x - 192;
         const int c = u & 15, rg = u >> 4;
         const bool live = 8 * c < head_dim;
-        const int64_t pairs = head_dim / 2;
-        const uint64_t tpol = policy_evict_last();
+        const uint32_t row_bytes = static_cast<uint32_t>(head_dim / 2) * 4u;
         uint64_t ks[4];  // the head's column sums in rope_chunk's activation order
         int cur_h = -1;
         uint32_t it = 0;
@@ -219,18 +292,6 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
             const int h = t / tiles_per_head;
             const int n0 = (t % tiles_per_head) * kApplyTile;
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
-            float4 cv[8], sv[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int n = n0 + rg + 16 * k;
-                if (live && n < n_tokens) {
-                    cv[k] = ldg_f4_hint(pa.cos + n * pairs + 4 * c, tpol);
-                    sv[k] = ldg_f4_hint(pa.sin + n * pairs + 4 * c, tpol);
-                } else {
-                    cv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    sv[k] = cv[k];
-                }
-            }
             if (h != cur_h) {
                 if (cur_h < 0) grid_dependency_wait();  // the column sums come from the reduction
                 cur_h = h;
@@ -246,31 +307,43 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
             if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
             if (!mbar_wait(den_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
             uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kQAtomBytes;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int r = rg + 16 * k;
-                const int n = n0 + r;
-                float part = 0.f;
-                if (live && n < n_tokens) {
-                    uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-                    uint4 w = *cell;
-                    uint64_t a0[2], a1[2];
-                    rope_chunk(w, cv[k], sv[k], a0, a1);
-                    uint64_t d2 = f32x2_mul(a0[0], ks[0]);
-                    d2 = f32x2_fma(a0[1], ks[1], d2);
-                    d2 = f32x2_fma(a1[0], ks[2], d2);
-                    d2 = f32x2_fma(a1[1], ks[3], d2);
-                    float d0, d1;
-                    f32x2_unpack(d2, d0, d1);
-                    part = d0 + d1;
-                    *cell = w;
+            bool ok = true;
+            const int kper = tab_rows / 16;  // this thread's rows per slot (rows rg + 16 k)
+            for (uint32_t hh = 0; hh < tab_subs; ++hh) {
+                const uint32_t i = tab_subs * it + hh;
+                const uint32_t slot = i & 1u;
+                if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i >> 1) & 1u, abort_flag, status))) break;
+                const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;
+                for (int k = kper * static_cast<int>(hh); k < kper * static_cast<int>(hh + 1); ++k) {
+                    const int r = rg + 16 * k;
+                    const int n = n0 + r;
+                    float part = 0.f;
+                    if (live && n < n_tokens) {
+                        const uint32_t tr = static_cast<uint32_t>(r - static_cast<int>(hh) * tab_rows) * row_bytes;
+                        const float4 c4 = *reinterpret_cast<const float4*>(tab + tr);
+                        const float4 s4 = *reinterpret_cast<const float4*>(tab + tab_slot / 2 + tr);
+                        uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                        uint4 w = *cell;
+                        uint64_t a0[2], a1[2];
+                        rope_chunk(w, c4, s4, a0, a1);
+                        uint64_t d2 = f32x2_mul(a0[0], ks[0]);
+                        d2 = f32x2_fma(a0[1], ks[1], d2);
+                        d2 = f32x2_fma(a1[0], ks[2], d2);
+                        d2 = f32x2_fma(a1[1], ks[3], d2);
+                        float d0, d1;
+                        f32x2_unpack(d2, d0, d1);
+                        part = d0 + d1;
+                        *cell = w;
+                    }
+                    part += __shfl_xor_sync(0xffffffffu, part, 8);
+                    part += __shfl_xor_sync(0xffffffffu, part, 4);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    if (c == 0) den_s[buf * kApplyTile + r] = part + kDenEps;
                 }
-                part += __shfl_xor_sync(0xffffffffu, part, 8);
-                part += __shfl_xor_sync(0xffffffffu, part, 4);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                if (c == 0) den_s[buf * kApplyTile + r] = part + kDenEps;
+                mbar_arrive(tab_empty0 + 8u * slot);
             }
+            if (!ok) break;
             fence_proxy_async_smem();
             mbar_arrive(q_ready0 + 8u * st);
             mbar_arrive(den_full0 + 8u * buf);
@@ -278,7 +351,7 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     } else if (!FUSED || warp < 6) {
         // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes / tile rows 32q..32q+31
         const int q = warp & 3;
-        const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
+        const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * kOutBufs * kOutBoxBytes;
         uint32_t nstore = 0;
         const uint64_t spol = policy_evict_first();
         constexpr int kCols = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
@@ -328,8 +401,8 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
                         }
                     }
                 }
-                const uint32_t sbuf = stage0 + (nstore & 1u) * kOutBoxBytes;
-                if (lane == 0) bulk_wait_read<1>();
+                const uint32_t sbuf = stage0 + (nstore % kOutBufs) * kOutBoxBytes;
+                if (lane == 0) bulk_wait_read<kOutBufs - 1>();
                 __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {

@@ -91,11 +91,11 @@ struct Strides {
 };
 
 // Number of 64-wide column blocks ("atoms") that cover the head dim: 1 for D <= 64, else 2.
-__host__ __device__ inline int head_dim_atoms(int head_dim) { return (head_dim + 63) / 64; }
+__host__ __device__ constexpr int head_dim_atoms(int head_dim) { return (head_dim + 63) / 64; }
 
 // Bytes of one head's three-term BF16 image of KV^T in the 128-byte-swizzled K-major
 // layout the apply kernel's MMA reads straight from shared memory.
-__host__ __device__ inline int64_t kv_image_bytes(int head_dim) {
+__host__ __device__ constexpr int64_t kv_image_bytes(int head_dim) {
     return 3ll * head_dim_atoms(head_dim) * head_dim * 128;
 }
 
