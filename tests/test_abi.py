@@ -82,20 +82,22 @@ def test_calls_on_null_context_are_rejected(la):
 
 def test_kv_plan_depends_on_shape_and_tier_only(la):
     # The plan fixes the summation order: a pure function of (H, N, tier) that keeps every
-    # head within the reduction's 160-partial budget.  Chunks of the (head, 64-token tile)
-    # sequence: G = min(target, tiles, 150 H); a head meets at most ceil(G / H) + 1 chunks.
-    for H in (1, 2, 12, 20, 32, 64, 4096):
+    # head within the reduction's 160-partial budget.  Each head's 64-token tiles are cut
+    # into k = max(1, min(152 // H, tiles per head, 150)) chunks at the same token
+    # boundaries for every head: G = k H chunks, k partials per head.
+    for H in (1, 2, 12, 20, 32, 64, 151, 152, 153, 4096):
         for N in (1, 63, 64, 65, 256, 1000, 32760, 180320, 262144):
             if H * N >= 2 ** 31:
                 continue
-            for mode, target in (("high", 152), ("lossless", 152)):
+            for mode in ("high", "lossless"):
                 G, segs = la.kv_plan(H, N, mode)
                 assert (G, segs) == la.kv_plan(H, N, mode)
-                T = H * -(-N // 64)
-                assert G == min(target, T, 150 * H)
-                assert 1 <= segs <= -(-G // H) + 1 <= 160
-    assert la.kv_plan(20, 180320, "high") == (152, 9)
-    assert la.kv_plan(20, 180320, "lossless") == (152, 9)
+                k = max(1, min(152 // H, -(-N // 64), 150))
+                assert (G, segs) == (k * H, k)
+                assert 1 <= segs <= 160
+    assert la.kv_plan(20, 180320, "high") == (140, 7)
+    assert la.kv_plan(20, 180320, "lossless") == (140, 7)
+    assert la.kv_plan(32, 180320, "high") == (128, 4)
     with pytest.raises(la.LinAttnError):
         la.kv_plan(0, 10, "high")
 

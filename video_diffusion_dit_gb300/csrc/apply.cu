@@ -8,6 +8,8 @@
 // reciprocal once and the row is multiplied by it (within 1 ulp of a true division).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "lin_attn_internal.cuh"
 #include "ptx.cuh"
 
@@ -109,9 +111,19 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = heads * tiles_per_head;
-    const int t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-    const int t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    // Head-major activations: contiguous ranges of the layer's (head, tile) sequence.
+    // Token-major: gridDim = k heads, CTA b takes part b % k of head b / k, every head cut
+    // at the same tiles, so the CTAs running together read and write the same token rows.
+    int t_begin, t_end;
+    if (!token_major) {
+        const int total = heads * tiles_per_head;
+        t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+        t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        const int k = gridDim.x / heads, hb = blockIdx.x / k, g = blockIdx.x % k;
+        t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k);
+        t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kApplyStages; ++s) {
@@ -468,8 +480,13 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
                             bool token_major, int grid, int* status, cudaStream_t stream,
                             const ProducerArgs* producer) {
     const int n = static_cast<int>(n_tokens);
-    const int total = heads * ((n + kApplyTile - 1) / kApplyTile);
+    const int tph = (n + kApplyTile - 1) / kApplyTile;
+    const int total = heads * tph;
     if (grid > total) grid = total;
+    if (token_major) {  // a whole number of CTAs per head (see the kernel's schedule)
+        const int k = std::max(1, std::min(grid / heads, tph));
+        grid = k * heads;
+    }
     const bool one = head_dim_atoms(head_dim) == 1;
     if (one)
         return out_bf16 ? launch_tc_any<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream, producer)

@@ -15,52 +15,60 @@ namespace la {
 constexpr int kKvTile = 64;
 // Token tile of the tensor-core apply kernel (MMA M).
 constexpr int kApplyTile = 128;
-// Work chunks of the KV reduction.  The layer's (head, 64-token tile) sequence, heads
-// outermost, is cut into G equal contiguous chunks; each chunk is summed by one CTA and
-// leaves one partial KV per head it touches.  G is a constant of the kernel (152 = one
-// chunk per SM of a 152-SM part), never read from the device, so the summation order is
-// fixed by the shape.
+// Work chunks of the KV reduction.  Each head's 64-token tiles are cut into k contiguous
+// chunks of equal size (+-1 tile), at the same token boundaries for every head:
+// k = min(floor(152 / H), tiles per head, 150), at least 1, and G = k H chunks in head
+// order (chunk c is part c % k of head c / k).  Each chunk is summed by one CTA and leaves
+// one partial KV.  With every head cut at the same tokens, the CTAs that run at the same
+// time walk the same token rows of all heads, which keeps reads of token-major [N, H, D]
+// activations on whole DRAM rows.  k and G are constants of the shape (152 = one chunk per
+// SM of a 152-SM part), never read from the device, so the summation order is fixed by the
+// shape.
 constexpr int kChunks = 152;
-constexpr int kChunksPerHeadCap = 150;  // G <= 150 * H keeps a head under kMaxSegments partials
+constexpr int kChunksPerHeadCap = 150;  // k <= 150 keeps a head under kMaxSegments partials
 constexpr int kMaxSegments = 160;       // partials per head the reduction can add
 
 struct KvPlan {
     int64_t tiles_per_head;  // ceil(N / kKvTile)
     int64_t total_tiles;     // H * tiles_per_head
-    int chunks;              // G
-    int seg_stride;          // partial slots per head: ceil(G / H) + 1 >= segments of any head
+    int chunks;              // G = k H
+    int per_head;            // k: chunks (and partials) per head
+    int seg_stride;          // partial slots per head (= k)
 };
 
+__host__ __device__ inline int kv_chunks_per_head(int heads, int64_t tiles_per_head) {
+    int64_t k = kChunks / heads;
+    if (k > tiles_per_head) k = tiles_per_head;
+    if (k > kChunksPerHeadCap) k = kChunksPerHeadCap;
+    return k < 1 ? 1 : static_cast<int>(k);
+}
 __host__ __device__ inline KvPlan kv_plan(int heads, int64_t n_tokens) {
     KvPlan p;
     p.tiles_per_head = (n_tokens + kKvTile - 1) / kKvTile;
     p.total_tiles = p.tiles_per_head * heads;
-    int64_t g = kChunks;
-    if (g > p.total_tiles) g = p.total_tiles;
-    if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
-    p.chunks = static_cast<int>(g);
-    p.seg_stride = (p.chunks + heads - 1) / heads + 1;
+    p.per_head = kv_chunks_per_head(heads, p.tiles_per_head);
+    p.chunks = p.per_head * heads;
+    p.seg_stride = p.per_head;
     return p;
 }
 // First tile of chunk c (chunk c covers [chunk_begin(c), chunk_begin(c + 1))).
-__host__ __device__ inline int64_t chunk_begin(const KvPlan& p, int64_t c) { return c * p.total_tiles / p.chunks; }
+__host__ __device__ inline int64_t chunk_begin(const KvPlan& p, int64_t c) {
+    const int64_t h = c / p.per_head, g = c % p.per_head;
+    return h * p.tiles_per_head + g * p.tiles_per_head / p.per_head;
+}
 // The chunk that holds tile t.
 __host__ __device__ inline int64_t chunk_of_tile(const KvPlan& p, int64_t t) {
-    return ((t + 1) * p.chunks - 1) / p.total_tiles;
+    const int64_t h = t / p.tiles_per_head, lt = t % p.tiles_per_head;
+    return h * p.per_head + ((lt + 1) * p.per_head - 1) / p.tiles_per_head;
 }
 // Partial slot of (head h, chunk c) and the number of partials of head h.
 __host__ __device__ inline int segment_of(const KvPlan& p, int h, int64_t c) {
-    return static_cast<int>(c - chunk_of_tile(p, h * p.tiles_per_head));
+    return static_cast<int>(c - static_cast<int64_t>(h) * p.per_head);
 }
-__host__ __device__ inline int segments_of_head(const KvPlan& p, int h) {
-    return static_cast<int>(chunk_of_tile(p, (h + 1) * p.tiles_per_head - 1) - chunk_of_tile(p, h * p.tiles_per_head) +
-                            1);
-}
+__host__ __device__ inline int segments_of_head(const KvPlan& p, int) { return p.per_head; }
 // Largest seg_stride any n_tokens can produce for `heads` (scratch sizing).
 __host__ __device__ inline int kv_seg_stride_bound(int heads) {
-    int64_t g = kChunks;
-    if (g > static_cast<int64_t>(kChunksPerHeadCap) * heads) g = static_cast<int64_t>(kChunksPerHeadCap) * heads;
-    return static_cast<int>((g + heads - 1) / heads + 1);
+    return kv_chunks_per_head(heads, static_cast<int64_t>(kChunksPerHeadCap));
 }
 
 // Work of one launch of the KV reduction: heads [h0, h0 + hc) of the layer (the K/V
