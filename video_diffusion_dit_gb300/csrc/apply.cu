@@ -50,12 +50,20 @@ constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
 // tab_rows consecutive tokens: half a tile where that fits in shared memory, else a quarter.
 constexpr uint32_t kSmemLimit = 232448;
 
+// Q stages: a one-atom tile (D <= 64) is half the bytes, so twice the stages keep as many
+// bytes in flight.
+__host__ __device__ constexpr int apply_stages(int nbox, bool fused) {
+    return fused ? (nbox == 1 ? 2 * kApplyStagesFused : kApplyStagesFused)
+                 : (nbox == 1 ? 2 * kApplyStagesPlain : kApplyStagesPlain);
+}
+constexpr uint32_t kApplyBarBytes = 512;  // mbarriers, TMEM address, abort flag
+
 __host__ __device__ constexpr uint32_t apply_smem_bytes_with(int head_dim, bool fused, int tab_rows) {
     const uint32_t nbox = head_dim_atoms(head_dim);
-    return static_cast<uint32_t>(kv_image_bytes(head_dim)) +
-           (fused ? kApplyStagesFused : kApplyStagesPlain) * nbox * kQAtomBytes +
+    return static_cast<uint32_t>(kv_image_bytes(head_dim)) + apply_stages(nbox, fused) * nbox * kQAtomBytes +
            4 * (fused ? kOutBufsFused : 2) * kOutBoxBytes +
-           (fused ? 2u * tab_rows * (head_dim / 2) * 4u * 2u : 0u) + 256 + (fused ? 2 * kApplyTile * 4 : 0) + 1024;
+           (fused ? 2u * tab_rows * (head_dim / 2) * 4u * 2u : 0u) + kApplyBarBytes +
+           (fused ? 2 * kApplyTile * 4 : 0) + 1024;
 }
 __host__ __device__ constexpr int apply_tab_rows(int head_dim) {
     return apply_smem_bytes_with(head_dim, true, LA_FUSED_TAB_ROWS_MAX) <= kSmemLimit ? LA_FUSED_TAB_ROWS_MAX
@@ -65,7 +73,8 @@ __host__ __device__ constexpr uint32_t apply_smem_bytes(int head_dim, bool fused
     return apply_smem_bytes_with(head_dim, fused, fused ? apply_tab_rows(head_dim) : 0);
 }
 // The largest head dim must fit, with whole 16-row groups of table rows per slot.
-static_assert(apply_smem_bytes(128, true) <= kSmemLimit && apply_smem_bytes(128, false) <= kSmemLimit,
+static_assert(apply_smem_bytes(128, true) <= kSmemLimit && apply_smem_bytes(128, false) <= kSmemLimit &&
+                  apply_smem_bytes(64, true) <= kSmemLimit && apply_smem_bytes(64, false) <= kSmemLimit,
               "apply layout exceeds shared memory");
 static_assert(apply_tab_rows(128) >= 16 && apply_tab_rows(16) % 16 == 0, "table slots must hold 16-row groups");
 
@@ -79,7 +88,7 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
 
-    constexpr int kApplyStages = FUSED ? kApplyStagesFused : kApplyStagesPlain;
+    constexpr int kApplyStages = apply_stages(NBOX, FUSED);
     constexpr uint32_t kOutBufs = FUSED ? kOutBufsFused : 2u;  // staging buffers per epilogue warp
     const uint32_t img_bytes = 3u * NBOX * head_dim * 128u;
     const uint32_t term_bytes = NBOX * head_dim * 128u;
@@ -104,9 +113,9 @@ __global__ void __launch_bounds__(FUSED ? kApplyThreadsFused : kApplyThreads, 1)
     const uint32_t den_empty0 = den_full0 + 16u;          // [2] (fused: row denominators read)
     const uint32_t tab_full0 = den_empty0 + 16u;          // [2] (fused: half-tile table rows landed)
     const uint32_t tab_empty0 = tab_full0 + 16u;          // [2] (fused: half-tile table rows used)
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + 200);
-    float* den_s = reinterpret_cast<float*>(base_ptr + bar_off + 256);  // fused: [2][kApplyTile]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + kApplyBarBytes - 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + kApplyBarBytes - 56);
+    float* den_s = reinterpret_cast<float*>(base_ptr + bar_off + kApplyBarBytes);  // fused: [2][kApplyTile]
     const uint32_t mma_ready0 = FUSED ? q_ready0 : q_full0;
 
     const int warp = threadIdx.x >> 5;
