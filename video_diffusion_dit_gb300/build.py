@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblin_attn.so")
-SOURCES = ["lin_attn_api.cu", "kv_reduce.cu", "apply.cu", "no_alloc.cu", "anchor_attention.cu"]
+SOURCES = ["lin_attn_api.cu", "kv_reduce.cu", "apply.cu", "apply_fused.cu", "no_alloc.cu", "anchor_attention.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -98,7 +98,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // unused): dims (D, N, H), box (box_x, rows, 1).  Token-major ([N][heads_total][D], the map
 // covering `h` heads from `base`): dims (D, H, N), box (box_x, 1, rows).
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t d, int64_t n,
-             int64_t h, uint32_t box_x, uint32_t box_y, bool token_major = false, int64_t heads_total = 0) {
+             int64_t h, uint32_t box_x, uint32_t box_y, bool token_major = false, int64_t heads_total = 0,
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(h)};
@@ -114,7 +115,7 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return LIN_ATTN_OK;
 }
@@ -224,11 +225,21 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         CUtensorMap tq, to;
         int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
         if (rc) return rc;
-        rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
-                      : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
-        if (rc) return rc;
-        e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream,
-                                fused ? &pa_apply : nullptr);
+        if (fused) {  // transposed epilogue: (32 features, 32 tokens) boxes, unswizzled
+            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 32, 32, false, 0,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE)
+                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, false, 0,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (rc) return rc;
+            e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream,
+                                          pa_apply);
+        } else {
+            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
+                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
+            if (rc) return rc;
+            e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream,
+                                    nullptr);
+        }
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     }
     if (ev && (e = cudaEventRecord(ev[3], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
