@@ -237,8 +237,7 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
             rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
             if (rc) return rc;
-            e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream,
-                                    nullptr);
+            e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream);
         }
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     }

@@ -219,8 +219,7 @@ cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_imag
 // out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms (maps as above).
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, cudaStream_t stream,
-                            const ProducerArgs* producer = nullptr);
+                            bool token_major, int grid, int* status, cudaStream_t stream);
 
 // Softmax anchor attention (flash forward): out = softmax(scale * Q K^T) V per head, no
 // mask.  Maps over [H][N][D] BF16: Q box (64, 128), K and V boxes (64, 64); scale_log2 =
