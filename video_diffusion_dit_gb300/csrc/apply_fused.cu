@@ -39,9 +39,13 @@ constexpr int kFXfWarp0 = 2 + kFEpiWarps;
 constexpr int kFThreads = 32 * (kFXfWarp0 + kFXfWarps);
 constexpr int kFTransformThreads = 32 * kFXfWarps;
 constexpr int kFRowGroups = kFTransformThreads / 16;  // a transform thread takes rows rg + kFRowGroups k
-constexpr int kFTabSlots = 3;                       // table ring: half-tile slots
+#ifndef LA_FUSED_TAB_SUBS
+#define LA_FUSED_TAB_SUBS 2
+#endif
+constexpr int kFTabSubs = LA_FUSED_TAB_SUBS;        // table slots per tile
+constexpr int kFTabSlots = 3 * kFTabSubs / 2;       // table ring: 1.5 tiles of rows
 constexpr uint32_t kFOutBufs = 1;                   // staging buffers per epilogue warp
-constexpr int kFTabRows = kApplyTile / 2;           // tokens per table slot
+constexpr int kFTabRows = kApplyTile / kFTabSubs;   // tokens per table slot
 constexpr uint32_t kFQAtom = kApplyTile * 128;      // 128 token rows x 128 bytes
 constexpr uint32_t kFBoxBytes = 32 * 128;           // staging box: 32 tokens x 128 bytes
 constexpr uint32_t kFBarBytes = 512;
@@ -61,6 +65,7 @@ __host__ __device__ constexpr uint32_t fused_smem_bytes(int head_dim) {
 static_assert(fused_smem_bytes(128) <= kFSmemLimit && fused_smem_bytes(64) <= kFSmemLimit,
               "fused apply layout exceeds shared memory");
 static_assert(kFImgCol + 3 * 64 <= 512, "accumulators and image exceed TMEM");
+static_assert(kFTabRows % (kFXfWarps * 32 / 16) == 0, "a table slot must hold whole row groups");
 
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
@@ -159,8 +164,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 q_issued = it + 1;
                 // The tile's rotation-table rows, half a tile per slot: rows of the [N][D/2]
                 // tables are contiguous, so a slot is one bulk copy per table, cut at N.
-                for (uint32_t hh = 0; hh < 2 && ok; ++hh) {
-                    const uint32_t i = 2u * it + hh;
+                for (uint32_t hh = 0; hh < kFTabSubs && ok; ++hh) {
+                    const uint32_t i = kFTabSubs * it + hh;
                     const uint32_t slot = i % kFTabSlots, tph = (i / kFTabSlots) & 1u;
                     if (!(ok = mbar_wait(tab_empty0 + 8u * slot, tph ^ 1u, abort_flag, status))) break;
                     const int r0 = n0 + static_cast<int>(hh) * kFTabRows;
@@ -261,8 +266,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
             uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kFQAtom;
             bool ok = true;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t i = 2u * it + hh;
+            for (int hh = 0; hh < kFTabSubs; ++hh) {
+                const uint32_t i = kFTabSubs * it + hh;
                 const uint32_t slot = i % kFTabSlots;
                 if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status))) break;
                 const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;

@@ -245,8 +245,11 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
     return ok();
 }
 
-// Heads per chunk of the host-buffer pipeline: about eight chunks per layer.
-int host_chunk_heads(int heads) { return heads >= 8 ? (heads + 7) / 8 : 1; }
+// Heads per chunk of the host-buffer pipeline: about twenty chunks per layer (finer
+// chunks expose less of the first upload and the last download; the kernels are cheap
+// beside the copies).
+constexpr int kHostChunks = 20;
+int host_chunk_heads(int heads) { return heads >= kHostChunks ? (heads + kHostChunks - 1) / kHostChunks : 1; }
 
 }  // namespace
 
