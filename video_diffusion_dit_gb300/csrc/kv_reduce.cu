@@ -29,7 +29,8 @@ namespace {
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
-constexpr int kKvThreadsFused = 320;  // + warps 6..9: the producer-step transform
+constexpr int kKvThreadsFused = 192 + 32 * kKsumGroups / 2;  // + warps 6..11: the producer-step transform
+constexpr int kKvTransformThreads = kKvThreadsFused - 192;
 // Tiles per tensor-core sub-chunk before its sum is promoted into FP32 registers: 4 (256
 // tokens) in the 'high' tier, 1 (64 tokens) in the 'lossless' tier.
 constexpr int kPromoteHigh = 4;
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         for (int s = 0; s < L::stages; ++s) {
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
-            if (FUSED) mbar_init(ready0 + 8u * s, 128);
+            if (FUSED) mbar_init(ready0 + 8u * s, kKvTransformThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
@@ -250,9 +251,9 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     const uint8_t* tab = stage + L::a_bytes + L::b_bytes + 16 * c;  // [64][pairs] floats
                     uint64_t ts[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int k8 = 0; k8 < kKvTile / 8; ++k8) {
-                        const int r = rg + 8 * k8;
-                        if (n0 + r < pa.n_tokens) {  // rows past the end stay zero
+                    for (int k = 0; k < (kKvTile + kKsumGroups - 1) / kKsumGroups; ++k) {
+                        const int r = rg + kKsumGroups * k;
+                        if (r < kKvTile && n0 + r < pa.n_tokens) {  // rows past the end stay zero
                             uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                             uint4 w = *cell;
                             const float4 c4 = *reinterpret_cast<const float4*>(tab + r * pairs * 4);
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             // reduction adds the 8 row groups in order, then the segments).
             if (live) {
                 const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
-                double* dst = pa.ksum_partial + (slot * 8 + rg) * head_dim + 8 * c;
+                double* dst = pa.ksum_partial + (slot * kKsumGroups + rg) * head_dim + 8 * c;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float s0, s1, c0, c1;
@@ -402,13 +403,13 @@ __device__ __forceinline__ float reduce_segments(const float* p, int64_t stride,
 // tile goes through shared memory so that 32 threads each write one 16-byte chunk (8
 // consecutive rows i of column j) per term of the image.
 // Fixed-order sum of a head's FP64 column-sum partials (fused path): each segment's value
-// is its 8 row-group sums added in order (p[s][0..7], `stride` apart), then the segments
-// are added with the same tree as above.
+// is its row-group sums added in order (p[s][0..kKsumGroups-1], `stride` apart), then the
+// segments are added with the same tree as above.
 __device__ __forceinline__ double segment_value_f64(const double* p, int64_t stride, int s) {
-    const double* q = p + static_cast<int64_t>(s) * 8 * stride;
+    const double* q = p + static_cast<int64_t>(s) * kKsumGroups * stride;
     double v = q[0];
 #pragma unroll
-    for (int g = 1; g < 8; ++g) v += q[g * stride];
+    for (int g = 1; g < kKsumGroups; ++g) v += q[g * stride];
     return v;
 }
 __device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t stride, int nseg) {
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
     const int nseg = segments_of_head(plan, h);
     if (ksum_partial != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < head_dim) {
         // Fused path: column sums of relu(K) over all tokens, rounded once to FP32.
-        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * 8 * head_dim + threadIdx.x;
+        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * kKsumGroups * head_dim + threadIdx.x;
         ksum[h * head_dim + threadIdx.x] = static_cast<float>(reduce_segments_f64(kp, head_dim, nseg));
     }
     float x = 0.f;

@@ -23,7 +23,7 @@ struct lin_attn_ctx {
     float* kv = nullptr;          // [heads][D][D] FP32 reduced KV
     uint8_t* kv_image = nullptr;  // [heads] x three-term BF16 image for the tensor-core apply
     int* status = nullptr;        // device status word (LIN_ATTN_ERR_TIMEOUT if a kernel gave up)
-    double* ksum_partial = nullptr;  // fused path: [heads][seg_stride_alloc][8][D] FP64 column sums of relu(K)
+    double* ksum_partial = nullptr;  // fused path: [heads][seg_stride_alloc][row groups][D] FP64 column sums of relu(K)
     float* ksum = nullptr;           // fused path: [heads][D] FP32 reduced column sums
     // host-buffer path staging, allocated on first use
     void* st_q = nullptr;
@@ -332,7 +332,7 @@ int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int h
                 cudaMalloc(&c->kv, sizeof(float) * dd * heads) == cudaSuccess &&
                 cudaMalloc(&c->kv_image, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads) == cudaSuccess &&
                 cudaMalloc(&c->status, sizeof(int)) == cudaSuccess &&
-                cudaMalloc(&c->ksum_partial, sizeof(double) * heads * c->seg_stride_alloc * 8 * head_dim) ==
+                cudaMalloc(&c->ksum_partial, sizeof(double) * heads * c->seg_stride_alloc * la::kKsumGroups * head_dim) ==
                     cudaSuccess &&
                 cudaMalloc(&c->ksum, sizeof(float) * heads * head_dim) == cudaSuccess;
     if (!good) {

@@ -132,9 +132,11 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 // The producer step fused into the tensor-core kernels (ReLU + interleaved RoPE on the
 // loaded Q / K tiles, the normaliser from the activated un-rotated copies).
 //   cos, sin : FP32 [N][D/2] rotation tables (pair p of token n is turned by cos/sin[n][p])
-//   ksum_partial : FP64 [H][seg_stride][8][D] per-chunk, per-row-group column sums of
-//                  relu(K) (scratch)
+//   ksum_partial : FP64 [H][seg_stride][kKsumGroups][D] per-chunk, per-row-group column
+//                  sums of relu(K) (scratch)
 //   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
+// Row groups of the fused KV kernel's transform (one column-sum partial each).
+constexpr int kKsumGroups = 12;
 struct ProducerArgs {
     const float* cos;
     const float* sin;
