@@ -79,23 +79,6 @@ __device__ __forceinline__ float half_weights(const uint32_t (&s)[64], uint64_t 
     return (a0 + a1) + (b0 + b1);
 }
 
-// Keys of a 64-column half past `valid` (relative to the half) become -inf.
-__device__ __forceinline__ void mask_half(uint32_t (&s)[64], int valid) {
-    if (valid < 64) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-            if (c >= valid) s[c] = __float_as_uint(-INFINITY);
-    }
-}
-
-__device__ __forceinline__ float half_max(const uint32_t (&s)[64]) {
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int c = 0; c < 64; c += 2)
-        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-}
-
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     anchor_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -257,15 +240,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = mbar_wait(s_full0 + 8u * t, j & 1u, abort_flag, status))) break;
             tc_fence_after();
-            // Row maximum over both 64-key halves; keep the upper half in registers.
-            const int valid = min(kBN, n_tokens - j * kBN);  // keys past the end are masked out
-            uint32_t s[64];
-            tmem_ld64_sync(s_addr, s);
-            mask_half(s, valid);
-            const float mx_lo = half_max(s);
-            tmem_ld64_sync(s_addr + 64u, s);
-            mask_half(s, valid - 64);
-            const float m_tile = fmaxf(mx_lo, half_max(s)) * scale_log2;
+            // The whole row of S_t(j); keys past the end are masked out.
+            const int valid = min(kBN, n_tokens - j * kBN);
+            uint32_t s[kBN];
+            tmem_ld128_sync(s_addr, s);
+            if (valid < kBN) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (c >= valid) s[c] = __float_as_uint(-INFINITY);
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < kBN; c += 2)
+                mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
             if (j == 0) {
                 m_ref = m_tile;
             } else {
@@ -288,14 +276,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
             }
-            // P_t(j) over S_t(j)'s columns 64..127: first the weights of keys 64..127 (their
-            // P columns 96..127 hold S values already in registers), then keys 0..63 from a
-            // second load of S columns 0..63 (their P columns 64..95 are consumed S too).
+            // P_t(j) over S_t(j)'s columns 64..127, all of whose S values are in registers:
+            // keys 64..127 to columns 96..127, then keys 0..63 to columns 64..95.
             const uint64_t scale2 = f32x2_pack(scale_log2, scale_log2), neg_m2 = f32x2_pack(-m_ref, -m_ref);
-            l += half_weights(s, scale2, neg_m2, s_addr + kPCol + 32u);
-            tmem_ld64_sync(s_addr, s);
-            mask_half(s, valid);
-            l += half_weights(s, scale2, neg_m2, s_addr + kPCol);
+            l += half_weights(*reinterpret_cast<const uint32_t(*)[64]>(s + 64), scale2, neg_m2, s_addr + kPCol + 32u);
+            l += half_weights(*reinterpret_cast<const uint32_t(*)[64]>(s), scale2, neg_m2, s_addr + kPCol);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(p_full0 + 8u * t);
