@@ -179,14 +179,14 @@ int lin_attn_debug_kv(lin_attn_ctx *ctx, float *kv_out, struct CUstream_st *stre
 int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
 
 /*
- * Work split of the KV reduction for this shape and tier.  The layer's (head, 64-token
- * tile) sequence, heads outermost, is cut into `*chunks` equal contiguous chunks (one CTA
- * each); every chunk leaves one partial D x D sum per head it touches, and each head's
- * partials (at most `*max_segments` for the busiest head) are added in a fixed pairwise
- * order.  The split depends on (heads, n_tokens) only - never on the GPU - which is what
- * makes the summation order, and so the result, reproducible (both tiers use the same
- * split).  Either out-pointer may be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad
- * arguments.
+ * Work split of the KV reduction for this shape and tier.  Each head's 64-token tiles
+ * are cut into k = min(152 / heads, tiles per head, 150) (at least 1) contiguous chunks of
+ * equal size, at the same token boundaries for every head; `*chunks` = k * heads (one CTA
+ * each), and each head's k partial D x D sums (`*max_segments` = k) are added in a fixed
+ * pairwise order.  The split depends on (heads, n_tokens) only - never on the GPU or the
+ * activation layout - which is what makes the summation order, and so the result,
+ * reproducible (both tiers and both layouts use the same split).  Either out-pointer may
+ * be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad arguments.
  */
 int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *max_segments);
 
