@@ -283,7 +283,7 @@ def run_ours(args, w, world, rank, local, dist):
               for i in range(args.layers)]
     if args.layout == "nhd":  # the model's [1, N, H, D] projection layout
         for g in layers:
-            for key in ("q_rot", "k_rot", "v"):
+            for key in ("q_rot", "k_rot", "v") + (("q", "k") if args.fused else ()):
                 g[key] = g[key].permute(0, 2, 1, 3).contiguous()
     layer = layers[0]
     out = torch.empty(1, H, N, D, dtype=out_dtype, device=dev)
@@ -295,7 +295,8 @@ def run_ours(args, w, world, rank, local, dist):
         g = layers[counter[0] % len(layers)]
         counter[0] += 1
         if args.fused:
-            ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out=out, stream=stream)
+            ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out=out, stream=stream,
+                              layout=args.layout)
         else:
             ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream,
                         layout=args.layout)
@@ -338,7 +339,8 @@ def run_ours(args, w, world, rank, local, dist):
 
     # ---- end to end through the host-buffer entry point (pinned host memory, [1, H, N, D])
     if args.layout == "nhd":
-        layer = {k: (t.permute(0, 2, 1, 3).contiguous() if k != "den" else t) for k, t in layer.items()}
+        layer = {k: (t.permute(0, 2, 1, 3).contiguous() if t.dim() == 4 and k != "den" else t)
+                 for k, t in layer.items()}
     host = {k: t.cpu().pin_memory() for k, t in layer.items()}
     hout = torch.empty(1, H, N, D, dtype=out_dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, args.e2e_steps))

@@ -128,12 +128,24 @@ int lin_attn_forward_layout(lin_attn_ctx *ctx, const void *q_rot, const void *k_
  * (x0 c - x1 s, x0 s + x1 c) with binary32 products and sums in exactly that order, rounded
  * once to BF16 (nearest-even); den[h][n] = qa[h][n] . (sum over m of ka[h][m]) + 1e-6; then
  * the two GEMMs and the normalisation of lin_attn_forward.  The column sums of relu(K) are
- * accumulated in FP64 and reduced in a fixed order.  mode must be LIN_ATTN_MODE_HIGH
+ * accumulated with compensated binary32 sums per chunk and reduced in FP64 in a fixed
+ * order, then rounded once to FP32.  mode must be LIN_ATTN_MODE_HIGH
  * (LIN_ATTN_ERR_UNSUPPORTED otherwise).
  */
 int lin_attn_forward_fused(lin_attn_ctx *ctx, const void *q, const void *k, const void *v,
                            const float *rope_cos, const float *rope_sin, void *out, int out_dtype,
                            int64_t n_tokens, int mode, struct CUstream_st *stream);
+
+/*
+ * lin_attn_forward_fused with a choice of activation layout.  LIN_ATTN_LAYOUT_NHD reads q,
+ * k, v as [1, N, H, D] (the per-head views of the model's packed projection output, page 1,
+ * 关键源码片段, `sana_video.py`: `.view(batch_size, sequence_length, num_heads, head_dim)`)
+ * and writes out as [1, N, H*D]; the rotation tables are per token in both layouts.  Same
+ * numbers as the head-major call (bitwise).  LIN_ATTN_ERR_INVALID_ARG for an unknown layout.
+ */
+int lin_attn_forward_fused_layout(lin_attn_ctx *ctx, const void *q, const void *k, const void *v,
+                                  const float *rope_cos, const float *rope_sin, void *out, int out_dtype,
+                                  int64_t n_tokens, int mode, int layout, struct CUstream_st *stream);
 
 /*
  * SANA-Video 2.0 softmax anchor layer (page "[sglang] SANA-Video 2.0 anchor attention의

@@ -65,6 +65,25 @@ def test_fused_small(la, dev, shape):
     check(la, dev, *shape, seed=shape[1])
 
 
+@pytest.mark.parametrize("shape", [(3, 777, 112), (2, 1000, 64), (4, 129, 128), (2, 65, 48)])
+def test_fused_token_major_is_bitwise_the_head_major_call(la, dev, shape):
+    # The model's projection layout [1, N, H, D] in, [1, N, H*D] out: the same plan and the
+    # same per-token arithmetic, so the same bits as the head-major fused call.
+    H, N, D = shape
+    g = {key: t.to(dev) for key, t in synth.make_layer(H, N, D, N + 1, producer_inputs=True).items()}
+    nhd = {key: g[key].permute(0, 2, 1, 3).contiguous() for key in ("q", "k", "v")}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for dt in (torch.float32, torch.bfloat16):
+            ref = ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out_dtype=dt).clone()
+            kv_ref = ctx.debug_kv().clone()
+            out = ctx.forward_fused(nhd["q"], nhd["k"], nhd["v"], g["rope_cos"], g["rope_sin"], out_dtype=dt,
+                                    layout="nhd")
+            assert ctx.device_status() == 0
+            assert tuple(out.shape) == (1, N, H * D)
+            assert torch.equal(ctx.debug_kv(), kv_ref)
+            assert torch.equal(out.reshape(1, N, H, D).permute(0, 2, 1, 3), ref)
+
+
 def test_fused_480p(la, dev):
     w = synth.WORKLOADS["480p_81f"]
     check(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid, dtypes=(torch.float32,))

@@ -2,6 +2,9 @@
 //     out[h][n][j] = (sum_i Q_rot[h][n][i] KV[h][i][j]) / den[h][n]
 //     as out^T = KV^T . Q_rot^T per 128-token tile (M = output feature j, N = token n)
 //
+// Activations may be head-major [1, H, N, D] or token-major [1, N, H, D] (the model's
+// projection layout); only the tensor-map coordinates and the schedule differ.
+//
 // Page "PR #35728 完整报告 - [diffusion] Accelerate SANA-Video linear attention in
 // quality=high", 关键源码片段: (scores @ query_rotate.float()) * normalizer, with the
 // producer step of SanaVideoLinearAttention.forward (ReLU, interleaved RoPE, the normaliser
@@ -71,7 +74,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
     apply_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                        const uint8_t* __restrict__ kv_image, int heads, int n_tokens, int head_dim,
-                       int tiles_per_head, int* status, const ProducerArgs pa) {
+                       int tiles_per_head, int token_major, int* status, const ProducerArgs pa) {
     constexpr int kStages = fused_stages(NBOX);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -102,9 +105,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = heads * tiles_per_head;
-    const int t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-    const int t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    // Head-major activations: contiguous ranges of the layer's (head, tile) sequence.
+    // Token-major: gridDim = k heads, CTA b takes part b % k of head b / k, every head cut
+    // at the same tiles, so the CTAs running together read and write the same token rows.
+    int t_begin, t_end;
+    if (!token_major) {
+        const int total = heads * tiles_per_head;
+        t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+        t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        const int k = gridDim.x / heads, hb = blockIdx.x / k, g = blockIdx.x % k;
+        t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k);
+        t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k);
+    }
     const uint32_t half_d = static_cast<uint32_t>(head_dim / 2);  // image columns per term
 
     if (threadIdx.x == 0) {
@@ -160,7 +173,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kFQAtom);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
-                    tma_load_3d_hint(q_smem + (st * NBOX + x) * kFQAtom, &tm_q, q_full0 + 8u * st, 64 * x, n0, h, pol);
+                    tma_load_3d_hint(q_smem + (st * NBOX + x) * kFQAtom, &tm_q, q_full0 + 8u * st, 64 * x,
+                                     token_major ? h : n0, token_major ? n0 : h, pol);
                 q_issued = it + 1;
                 // The tile's rotation-table rows, half a tile per slot: rows of the [N][D/2]
                 // tables are contiguous, so a slot is one bulk copy per table, cut at N.
@@ -394,7 +408,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d_hint(&tm_out, sbuf, 32 * q, n0 + 32 * g, h, spol);
+                    tma_store_3d_hint(&tm_out, sbuf, 32 * q, token_major ? h : n0 + 32 * g,
+                                      token_major ? n0 + 32 * g : h, spol);
                     bulk_commit();
                 }
                 ++nstore;
@@ -419,29 +434,34 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
 template <int NBOX, bool BF16>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, int heads, int n_tokens,
-                   int head_dim, int grid, int* status, cudaStream_t stream, const ProducerArgs& pa) {
+                   int head_dim, bool token_major, int grid, int* status, cudaStream_t stream, const ProducerArgs& pa) {
     const uint32_t smem = fused_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_fused_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
     return launch_overlapped(apply_fused_kernel<NBOX, BF16>, dim3(grid), dim3(kFThreads), smem, stream, tm_q, tm_out,
-                             img, heads, n_tokens, head_dim, tph, status, pa);
+                             img, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, pa);
 }
 
 }  // namespace
 
 cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out_t, const uint8_t* kv_image,
-                                  int heads, int64_t n_tokens, int head_dim, bool out_bf16, int grid, int* status,
-                                  cudaStream_t stream, const ProducerArgs& producer) {
+                                  int heads, int64_t n_tokens, int head_dim, bool out_bf16, bool token_major, int grid,
+                                  int* status, cudaStream_t stream, const ProducerArgs& producer) {
     const int n = static_cast<int>(n_tokens);
-    const int total = heads * ((n + kApplyTile - 1) / kApplyTile);
+    const int tph = (n + kApplyTile - 1) / kApplyTile;
+    const int total = heads * tph;
     if (grid > total) grid = total;
+    if (token_major) {  // a whole number of CTAs per head (see the kernel's schedule)
+        const int k = grid / heads < 1 ? 1 : (grid / heads < tph ? grid / heads : tph);
+        grid = k * heads;
+    }
     if (head_dim_atoms(head_dim) == 1)
-        return out_bf16 ? launch<1, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, grid, status, stream, producer)
-                        : launch<1, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, grid, status, stream, producer);
-    return out_bf16 ? launch<2, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, grid, status, stream, producer)
-                    : launch<2, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, grid, status, stream, producer);
+        return out_bf16 ? launch<1, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer)
+                        : launch<1, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer);
+    return out_bf16 ? launch<2, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer)
+                    : launch<2, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer);
 }
 
 }  // namespace la

@@ -226,13 +226,13 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
         if (rc) return rc;
         if (fused) {  // transposed epilogue: (32 features, 32 tokens) boxes, unswizzled
-            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 32, 32, false, 0,
+            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 32, 32, tm, H,
                                      CU_TENSOR_MAP_SWIZZLE_NONE)
-                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, false, 0,
+                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H,
                                      CU_TENSOR_MAP_SWIZZLE_NONE);
             if (rc) return rc;
-            e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, c->n_sms, c->status, stream,
-                                          pa_apply);
+            e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status,
+                                          stream, pa_apply);
         } else {
             rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
@@ -396,6 +396,15 @@ int lin_attn_forward_layout(lin_attn_ctx* ctx, const void* q_rot, const void* k_
 int lin_attn_forward_fused(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* rope_cos,
                            const float* rope_sin, void* out, int out_dtype, int64_t n_tokens, int mode,
                            struct CUstream_st* stream) {
+    return lin_attn_forward_fused_layout(ctx, q, k, v, rope_cos, rope_sin, out, out_dtype, n_tokens, mode,
+                                         LIN_ATTN_LAYOUT_HND, stream);
+}
+
+int lin_attn_forward_fused_layout(lin_attn_ctx* ctx, const void* q, const void* k, const void* v,
+                                  const float* rope_cos, const float* rope_sin, void* out, int out_dtype,
+                                  int64_t n_tokens, int mode, int layout, struct CUstream_st* stream) {
+    if (layout != LIN_ATTN_LAYOUT_HND && layout != LIN_ATTN_LAYOUT_NHD)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "layout=%d is not LIN_ATTN_LAYOUT_HND/NHD", layout);
     if (!rope_cos || !rope_sin) return fail(LIN_ATTN_ERR_INVALID_ARG, "rotation table pointer is NULL");
     // check_call wants a denominator pointer; the fused call forms the denominators itself.
     int rc = check_call(ctx, q, k, v, rope_cos, out, out_dtype, n_tokens, mode);
@@ -410,7 +419,7 @@ int lin_attn_forward_fused(lin_attn_ctx* ctx, const void* q, const void* k, cons
     cudaEvent_t* ev = ctx->n_events == 4 ? ctx->events : nullptr;
     ctx->n_events = 0;
     return enqueue_heads(ctx, q, k, v, nullptr, out, out_dtype, n_tokens, mode, reinterpret_cast<cudaStream_t>(stream),
-                         0, ctx->heads, ev, LIN_ATTN_LAYOUT_HND, rope_cos, rope_sin);
+                         0, ctx->heads, ev, layout, rope_cos, rope_sin);
 }
 
 int lin_attn_anchor_forward(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, void* out,

@@ -227,11 +227,11 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
 // mask.  Maps over [H][N][D] BF16: Q box (64, 128), K and V boxes (64, 64); scale_log2 =
 // scale * log2(e).
 // Second GEMM of the fused producer path, computed as out^T = KV^T Q_rot^T with the KV
-// image in TMEM (head-major activations only).  tm_q as for launch_apply_tc; tm_out_t maps
-// out with a (32 features, 32 tokens) box and no swizzle.
+// image in TMEM.  tm_q as for launch_apply_tc; tm_out_t maps out with a (32 features,
+// 32 tokens) box and no swizzle; both index (column, head, token) if token_major.
 cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out_t, const uint8_t* kv_image,
-                                  int heads, int64_t n_tokens, int head_dim, bool out_bf16, int grid, int* status,
-                                  cudaStream_t stream, const ProducerArgs& producer);
+                                  int heads, int64_t n_tokens, int head_dim, bool out_bf16, bool token_major, int grid,
+                                  int* status, cudaStream_t stream, const ProducerArgs& producer);
 
 cudaError_t launch_anchor_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     void* out, bool out_bf16, int heads, int64_t n_tokens, int head_dim,

@@ -22,7 +22,7 @@ EXPORTS = (
     "lin_attn_create", "lin_attn_destroy", "lin_attn_forward", "lin_attn_forward_layout", "lin_attn_forward_host",
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
-    "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward",
+    "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward", "lin_attn_forward_fused_layout",
 )
 
 
@@ -46,6 +46,7 @@ def _load():
         "lin_attn_version": ([], i32),
         "lin_attn_forward_noalloc": ([p, p, p, p, p, i32, i32, i64, i32, i32, p], i32),
         "lin_attn_forward_fused": ([p, p, p, p, p, p, p, i32, i64, i32, p], i32),
+        "lin_attn_forward_fused_layout": ([p, p, p, p, p, p, p, i32, i64, i32, i32, p], i32),
         "lin_attn_anchor_forward": ([p, p, p, p, p, i32, i64, ctypes.c_float, p], i32),
     }
     for name, (args, res) in sig.items():
@@ -188,15 +189,25 @@ class LinAttn:
         _check(st, "lin_attn_forward")
         return out
 
-    def forward_fused(self, q, k, v, rope_cos, rope_sin, out=None, out_dtype=torch.float32, stream=None):
-        """Layer call from the pre-activation q, k ([1, H, N, D] BF16): ReLU, interleaved RoPE
-        (FP32 tables [N, D/2]) and the normaliser run inside the kernels ('high' tier)."""
+    def forward_fused(self, q, k, v, rope_cos, rope_sin, out=None, out_dtype=torch.float32, stream=None,
+                      layout="hnd"):
+        """Layer call from the pre-activation q, k: ReLU, interleaved RoPE (FP32 tables
+        [N, D/2]) and the normaliser run inside the kernels ('high' tier).
+
+        layout "hnd": q, k, v and out are [1, H, N, D].
+        layout "nhd": q, k, v are [1, N, H, D] (the model's projection layout) and out is
+        [1, N, H*D] (any contiguous tensor of that many elements is accepted)."""
         for name, t in (("q", q), ("k", k), ("v", v)):
             if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != self.device:
                 raise ValueError(f"{name} must be a contiguous bfloat16 tensor on {self.device}")
         if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.shape[0] != 1:
-            raise ValueError("q, k, v must share one [1, H, N, D] shape")
-        _, H, N, D = q.shape
+            raise ValueError("q, k, v must share one 4-D shape with batch 1")
+        if layout == "hnd":
+            _, H, N, D = q.shape
+        elif layout == "nhd":
+            _, N, H, D = q.shape
+        else:
+            raise ValueError(f"layout must be 'hnd' or 'nhd', got {layout!r}")
         if H != self.heads or D != self.head_dim:
             raise ValueError(f"context is for H={self.heads}, D={self.head_dim}; got H={H}, D={D}")
         for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
@@ -204,12 +215,14 @@ class LinAttn:
                     or t.device != self.device:
                 raise ValueError(f"{name} must be a contiguous float32 [{N}, {D // 2}] tensor on {self.device}")
         if out is None:
-            out = torch.empty(q.shape, dtype=out_dtype, device=self.device)
-        elif out.shape != q.shape or not out.is_contiguous() or out.device != self.device:
-            raise ValueError("out must be a contiguous [1, H, N, D] tensor on the context's device")
-        st = lib.lin_attn_forward_fused(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
-                                        rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N, MODE_HIGH,
-                                        _stream_handle(stream, self.device))
+            shape = q.shape if layout == "hnd" else (1, N, H * D)
+            out = torch.empty(shape, dtype=out_dtype, device=self.device)
+        elif out.numel() != q.numel() or not out.is_contiguous() or out.device != self.device:
+            raise ValueError("out must be a contiguous tensor of the inputs' size on the context's device")
+        st = lib.lin_attn_forward_fused_layout(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
+                                               rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N, MODE_HIGH,
+                                               LAYOUT_HND if layout == "hnd" else LAYOUT_NHD,
+                                               _stream_handle(stream, self.device))
         _check(st, "lin_attn_forward_fused")
         return out
 
