@@ -154,6 +154,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def call_percentiles(step, steps, stream, dev):
+    """p10 / p50 / p90 of the per-call time (ms), each call bracketed by its own events."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t = np.array([a.elapsed_time(b) for a, b in ev])
+    p10, p50, p90 = np.percentile(t, [10, 50, 90])
+    return {"p10": float(p10), "p50": float(p50), "p90": float(p90), "calls": steps,
+            "note": "a separate pass with an event pair around every call; the timed pass has no events"}
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -336,6 +351,7 @@ def run_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize(dev)
     stage_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                 for j, name in enumerate(("kv_partial", "kv_finalize", "apply"))}
+    call_ms = call_percentiles(step, min(args.steps, 500), stream, dev)
 
     # ---- end to end through the host-buffer entry point (pinned host memory, [1, H, N, D])
     if args.layout == "nhd":
@@ -380,6 +396,7 @@ def run_ours(args, w, world, rank, local, dist):
                 "producer": "fused (ReLU + RoPE + normaliser in the kernels)" if args.fused else "inputs pre-rotated",
             },
             "achieved_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
+            "call_ms": call_ms,
             "stage_ms": stage_ms,
             "roofline": {"kernel": kernel_names[dom], "bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -508,6 +525,7 @@ def run_anchor(args, w, world, rank, local, dist):
     sustained = elapsed_ms > 1000.0
     peak, peak_kind = load_tensor_peak(sustained)
     achieved = flops / (ms_per_step / 1e3) / 1e12
+    call_ms = call_percentiles(step, args.steps, stream, dev)
 
     # ---- end to end through the Python API: pinned host q, k, v in, out back to pinned host
     g = layers[0]
@@ -550,6 +568,7 @@ def run_anchor(args, w, world, rank, local, dist):
             "e2e": {"value": world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 3 * H * N * D * 2,
                     "d2h_bytes_per_step": H * N * D * out_bytes, "steps": e2e_steps},
             "gpu_launches": args.steps,
+            "call_ms": call_ms,
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }
