@@ -9,10 +9,10 @@
 // GEMM on BF16 operands is the FP32 GEMM on the upcast operands up to rounding; 'lossless'
 // promotes the tensor-core sums into FP32 registers four times as often.
 //
-// Work split (KvPlan): the layer's (head, 64-token tile) sequence is cut into G equal
-// contiguous chunks, one CTA each.  A chunk leaves one D x D partial sum per head it
-// touches (a "segment"); kv_finalize adds each head's partials in a fixed pairwise order.
-// G is a constant, so the order - and the result - depends on the shape alone.
+// Work split (KvPlan): each head's 64-token tiles are cut into k equal contiguous chunks,
+// at the same token boundaries for every head, one CTA each.  A chunk leaves one D x D
+// partial sum (a "segment"); kv_finalize adds each head's partials in a fixed pairwise
+// order.  k depends on the shape alone, and so do the order and the result.
 #include <cuda_bf16.h>
 
 #include "lin_attn_internal.cuh"
