@@ -311,7 +311,7 @@ def run_ours(args, w, world, rank, local, dist):
         counter[0] += 1
         if args.fused:
             ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out=out, stream=stream,
-                              layout=args.layout)
+                              layout=args.layout, mode=args.mode)
         else:
             ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=out, mode=args.mode, stream=stream,
                         layout=args.layout)

@@ -115,7 +115,7 @@ int lin_attn_forward_layout(lin_attn_ctx *ctx, const void *q_rot, const void *k_
                             int mode, int layout, struct CUstream_st *stream);
 
 /*
- * The layer call with the producer step fused in ('high' tier): what the model does right
+ * The layer call with the producer step fused in (either tier): what the model does right
  * before the two GEMMs (page 1, 关键源码片段, `sana_video.py`: `F.relu` on the normalised
  * query and key, `apply_interleaved_rotary_emb` on the activated copies, and the normaliser
  * from the un-rotated activated copies) runs inside the kernels, on the tiles they load.
@@ -129,8 +129,8 @@ int lin_attn_forward_layout(lin_attn_ctx *ctx, const void *q_rot, const void *k_
  * once to BF16 (nearest-even); den[h][n] = qa[h][n] . (sum over m of ka[h][m]) + 1e-6; then
  * the two GEMMs and the normalisation of lin_attn_forward.  The column sums of relu(K) are
  * accumulated with compensated binary32 sums per chunk and reduced in FP64 in a fixed
- * order, then rounded once to FP32.  mode must be LIN_ATTN_MODE_HIGH
- * (LIN_ATTN_ERR_UNSUPPORTED otherwise).
+ * order, then rounded once to FP32.  mode: LIN_ATTN_MODE_HIGH or LIN_ATTN_MODE_LOSSLESS, as
+ * for lin_attn_forward.
  */
 int lin_attn_forward_fused(lin_attn_ctx *ctx, const void *q, const void *k, const void *v,
                            const float *rope_cos, const float *rope_sin, void *out, int out_dtype,

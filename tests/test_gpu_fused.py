@@ -107,16 +107,41 @@ def test_fused_720p_sampled(la, dev):
         assert torch.equal(again, third)
 
 
-def test_fused_rejects_lossless_and_bad_tables(la, dev):
+def test_fused_rejects_bad_arguments(la, dev):
     g = {k: t.to(dev) for k, t in synth.make_layer(2, 64, 32, 0, producer_inputs=True).items()}
     with la.LinAttn(2, 64, 32, dev) as ctx:
         out = torch.empty(1, 2, 64, 32, device=dev)
         s = torch.cuda.current_stream().cuda_stream
         args = [g["q"].data_ptr(), g["k"].data_ptr(), g["v"].data_ptr(), g["rope_cos"].data_ptr(),
                 g["rope_sin"].data_ptr(), out.data_ptr(), la.OUT_F32, 64]
-        assert la.lib.lin_attn_forward_fused(ctx._h, *args, la.MODE_LOSSLESS, s) == la.ERR_UNSUPPORTED
+        assert la.lib.lin_attn_forward_fused(ctx._h, *args, 7, s) == la.ERR_INVALID_ARG
+        assert la.lib.lin_attn_forward_fused_layout(ctx._h, *args, la.MODE_HIGH, 5, s) == la.ERR_INVALID_ARG
         bad = list(args)
         bad[3] = 0
         assert la.lib.lin_attn_forward_fused(ctx._h, *bad, la.MODE_HIGH, s) == la.ERR_INVALID_ARG
         with pytest.raises(ValueError):
             ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"][:32], g["rope_sin"])
+        assert ctx.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(3, 777, 112), (2, 1000, 64), (4, 129, 128)])
+def test_fused_lossless(la, dev, shape):
+    # The 'lossless' tier with the producer step fused in: the oracle's numbers within the
+    # same tolerances, and bitwise the KV of the plain lossless call on the generator's
+    # rotated operands (the rotation is defined bit for bit).
+    H, N, D = shape
+    layer = synth.make_layer(H, N, D, 7 * N, producer_inputs=True)
+    ref, kv_ref = oracle_fused(layer)
+    ref = ref.reshape(H, N, D)
+    g = {key: t.to(dev) for key, t in layer.items()}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for dt in (torch.float32, torch.bfloat16):
+            out = ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out_dtype=dt,
+                                    mode="lossless")
+            assert ctx.device_status() == 0
+            err = rel_l2(out.double().cpu().numpy()[0], ref)
+            assert err <= TOL[dt], f"fused lossless H={H} N={N} D={D} {dt}: rel-L2 {err:.3e}"
+        kv_fused = ctx.debug_kv().clone()
+        assert rel_l2(kv_fused.double().cpu().numpy(), kv_ref) <= 1e-6
+        ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], mode="lossless")
+        assert torch.equal(ctx.debug_kv(), kv_fused)

@@ -527,6 +527,8 @@ cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_
     const bool one = head_dim_atoms(head_dim) == 1;
 #define LA_KV_LAUNCH(NB, FU, PR) \
     launch_tc<NB, FU, PR>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
+    if (producer && lossless)
+        return one ? LA_KV_LAUNCH(1, true, kPromoteLossless) : LA_KV_LAUNCH(2, true, kPromoteLossless);
     if (producer) return one ? LA_KV_LAUNCH(1, true, kPromoteHigh) : LA_KV_LAUNCH(2, true, kPromoteHigh);
     if (lossless) return one ? LA_KV_LAUNCH(1, false, kPromoteLossless) : LA_KV_LAUNCH(2, false, kPromoteLossless);
     return one ? LA_KV_LAUNCH(1, false, kPromoteHigh) : LA_KV_LAUNCH(2, false, kPromoteHigh);

@@ -409,8 +409,6 @@ int lin_attn_forward_fused_layout(lin_attn_ctx* ctx, const void* q, const void* 
     // check_call wants a denominator pointer; the fused call forms the denominators itself.
     int rc = check_call(ctx, q, k, v, rope_cos, out, out_dtype, n_tokens, mode);
     if (rc) return rc;
-    if (mode != LIN_ATTN_MODE_HIGH)
-        return fail(LIN_ATTN_ERR_UNSUPPORTED, "the fused producer step runs in LIN_ATTN_MODE_HIGH only");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
         !aligned16(out))
         return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");

@@ -190,9 +190,9 @@ class LinAttn:
         return out
 
     def forward_fused(self, q, k, v, rope_cos, rope_sin, out=None, out_dtype=torch.float32, stream=None,
-                      layout="hnd"):
+                      layout="hnd", mode="high"):
         """Layer call from the pre-activation q, k: ReLU, interleaved RoPE (FP32 tables
-        [N, D/2]) and the normaliser run inside the kernels ('high' tier).
+        [N, D/2]) and the normaliser run inside the kernels (either tier).
 
         layout "hnd": q, k, v and out are [1, H, N, D].
         layout "nhd": q, k, v are [1, N, H, D] (the model's projection layout) and out is
@@ -220,7 +220,7 @@ class LinAttn:
         elif out.numel() != q.numel() or not out.is_contiguous() or out.device != self.device:
             raise ValueError("out must be a contiguous tensor of the inputs' size on the context's device")
         st = lib.lin_attn_forward_fused_layout(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
-                                               rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N, MODE_HIGH,
+                                               rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N, _mode(mode),
                                                LAYOUT_HND if layout == "hnd" else LAYOUT_NHD,
                                                _stream_handle(stream, self.device))
         _check(st, "lin_attn_forward_fused")
