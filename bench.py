@@ -77,16 +77,17 @@ def anchor_flops(H, N, D):
     return 4 * H * N * N * D
 
 
-def kernel_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu capture, or None when the kernel
-    source changed since the capture (or no capture exists)."""
+def kernel_traffic(kernel, config):
+    """DRAM bytes per launch from the committed ncu capture, or None when the capture was
+    of another configuration (workload, tier, output type, layout, producer), the kernel
+    source changed since the capture, or no capture exists."""
     p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get("kernels", {}).get(kernel)
-    if not ent:
+    if not ent or d.get("config") != config:
         return None
     src = os.path.join(ROOT, ent["source"])
     if not os.path.exists(src):
@@ -378,7 +379,10 @@ def run_ours(args, w, world, rank, local, dist):
     peak, peak_kind = load_peaks()
     dom = max(("kv_partial", "apply"), key=lambda k: stage_ms[k])
     achieved = nbytes[dom] / (stage_ms[dom] / 1e3) / 1e9
-    kernel_names = {"kv_partial": "kv_partial_tc_kernel", "apply": "apply_tc_kernel"}
+    kernel_names = {"kv_partial": "kv_partial_tc_kernel",
+                    "apply": "apply_fused_kernel" if args.fused else "apply_tc_kernel"}
+    traffic_config = {"workload": w.name, "mode": args.mode, "out_dtype": args.out_dtype, "layout": args.layout,
+                      "fused": bool(args.fused)}
     result = None
     if rank == 0:
         cpu = cpu_baseline(layer_to_numpy(layer), H, N, args.cpu_budget) if (world == 1 and not args.no_cpu) else None
@@ -400,7 +404,7 @@ def run_ours(args, w, world, rank, local, dist):
             "stage_ms": stage_ms,
             "roofline": {"kernel": kernel_names[dom], "bound": "hbm", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": kernel_traffic(kernel_names[dom]),
+                         "traffic": kernel_traffic(kernel_names[dom], traffic_config),
                          "algorithmic_bytes": nbytes[dom]},
             "e2e": {"value": world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},

@@ -60,3 +60,19 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_is_reported_only_for_the_captured_configuration():
+    # The committed ncu byte counts belong to one configuration and one kernel source;
+    # any other configuration, or an edited source, reports null rather than a stale count.
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")) as f:
+        cap = json.load(f)
+    cfg = dict(cap["config"])
+    for kernel, ent in cap["kernels"].items():
+        assert bench.kernel_traffic(kernel, cfg) == ent["bytes_per_launch_full"]
+        for key, other in (("workload", "480p_81f"), ("mode", "lossless"), ("out_dtype", "bf16"),
+                           ("layout", "nhd"), ("fused", True)):
+            assert bench.kernel_traffic(kernel, {**cfg, key: other}) is None
+    assert bench.kernel_traffic("apply_fused_kernel", cfg) is None
