@@ -136,7 +136,10 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 //                  sums of relu(K) (scratch)
 //   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
 // Row groups of the fused KV kernel's transform (one column-sum partial each).
-constexpr int kKsumGroups = 12;
+#ifndef LA_KSUM_GROUPS
+#define LA_KSUM_GROUPS 12
+#endif
+constexpr int kKsumGroups = LA_KSUM_GROUPS;
 struct ProducerArgs {
     const float* cos;
     const float* sin;
@@ -177,25 +180,6 @@ __device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const floa
         act1[h] = f32x2_pack(x1[2 * h], x1[2 * h + 1]);
     }
     w = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-}
-
-// Rotation-table rows of one 8-row batch of the producer transform: rows row0 + rg + 8k,
-// k = 0..7, columns 8c..8c+7 (pairs 4c..4c+3).  Rows past the end (or dead chunks) get
-// zeros.  Issued a batch ahead of use so the L2 latency overlaps the transform.
-__device__ __forceinline__ void load_rope_rows(const float* cos, const float* sin, int64_t pairs, int c, int row0,
-                                               int rg, int n_tokens, bool live, uint64_t pol, float4 (&cv)[8],
-                                               float4 (&sv)[8]) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int n = row0 + rg + 8 * k;
-        if (live && n < n_tokens) {
-            cv[k] = ldg_f4_hint(cos + n * pairs + 4 * c, pol);
-            sv[k] = ldg_f4_hint(sin + n * pairs + 4 * c, pol);
-        } else {
-            cv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            sv[k] = cv[k];
-        }
-    }
 }
 
 // ---------------------------------------------------------------- launchers
