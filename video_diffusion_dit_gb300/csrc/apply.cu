@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             // Q tiles are inputs of the call and may be fetched before the reduction that
             // produces the KV image has finished; the image is loaded only after the wait.
             bool waited = false;
-            const uint64_t pol = policy_evict_first();
+            // Token-major Q rows share DRAM granules with the neighbouring heads' rows, which
+            // other CTAs read at about the same time: those lines stay at normal priority.
+            const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             bool ok = true, b_pending = false;
@@ -213,7 +215,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         const int q = warp & 3;
         const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
         uint32_t nstore = 0;
-        const uint64_t spol = policy_evict_first();
+        // Token-major output rows share L2 lines with the neighbouring heads' rows (written by
+        // other CTAs): normal priority, as for the loads.
+        const uint64_t spol = token_major ? policy_evict_normal() : policy_evict_first();
         constexpr int kCols = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
         const int groups = (head_dim + kCols - 1) / kCols;
         for (int t = t_begin; t < t_end; ++t) {

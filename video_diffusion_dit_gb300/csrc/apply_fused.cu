@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: Q tiles (inputs of the call) and table rows
-            const uint64_t pol = policy_evict_first();
+            // Token-major Q rows share DRAM granules with the neighbouring heads' rows, which
+            // other CTAs read at about the same time: those lines stay at normal priority.
+            const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             const uint64_t tpol = policy_evict_last();  // every head of the layer re-reads the tables
             const uint32_t row_bytes = half_d * 4u;
             uint32_t q_issued = 0, tab_issued = 0;  // copies issued (for the wind-down)
@@ -330,7 +332,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const bool live = 32 * q < head_dim;  // any of the warp's features exists
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * kFOutBufs * kFBoxBytes;
-        const uint64_t spol = policy_evict_first();
+        // Token-major output rows share L2 lines with the neighbouring heads' rows (written by
+        // other CTAs): normal priority, as for the loads.
+        const uint64_t spol = token_major ? policy_evict_normal() : policy_evict_first();
         const int64_t term_bytes = static_cast<int64_t>(NBOX) * head_dim * 128;
         uint32_t nstore = 0;
         int cur_h = -1, run = -1;

@@ -138,7 +138,9 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: every tile of the chunk, in order
-            const uint64_t pol = policy_evict_first();
+            // Token-major K/V rows share DRAM granules with the neighbouring heads' rows, which
+            // other CTAs read at about the same time: those lines stay at normal priority.
+            const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             const uint64_t tab_pol = policy_evict_last();
             uint32_t it = 0;
             bool ok = true;

@@ -104,6 +104,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
+// L2 policy for streamed data that other CTAs may read again shortly (token-major rows that
+// share DRAM granules with the neighbouring heads' rows).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 // L2 policy for small data every CTA re-reads (rotation tables): kept in L2 last.
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t pol;
