@@ -77,11 +77,11 @@ def anchor_flops(H, N, D):
     return 4 * H * N * N * D
 
 
-def kernel_traffic(kernel, config):
+def kernel_traffic(kernel, config, path=None):
     """DRAM bytes per launch from the committed ncu capture, or None when the capture was
     of another configuration (workload, tier, output type, layout, producer), the kernel
     source changed since the capture, or no capture exists."""
-    p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+    p = path or os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:

@@ -62,17 +62,30 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
 
 
-def test_traffic_is_reported_only_for_the_captured_configuration():
+def test_traffic_is_reported_only_for_the_captured_configuration(tmp_path):
     # The committed ncu byte counts belong to one configuration and one kernel source;
     # any other configuration, or an edited source, reports null rather than a stale count.
+    import hashlib
     sys.path.insert(0, ROOT)
     import bench
     with open(os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")) as f:
         cap = json.load(f)
     cfg = dict(cap["config"])
+    for ent in cap["kernels"].values():  # the same file, with the sources as they are now
+        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+            ent["source_sha256"] = hashlib.sha256(f.read()).hexdigest()
+    cur = tmp_path / "current.json"
+    cur.write_text(json.dumps(cap))
     for kernel, ent in cap["kernels"].items():
-        assert bench.kernel_traffic(kernel, cfg) == ent["bytes_per_launch_full"]
+        assert bench.kernel_traffic(kernel, cfg, str(cur)) == ent["bytes_per_launch_full"]
         for key, other in (("workload", "480p_81f"), ("mode", "lossless"), ("out_dtype", "bf16"),
                            ("layout", "nhd"), ("fused", True)):
-            assert bench.kernel_traffic(kernel, {**cfg, key: other}) is None
-    assert bench.kernel_traffic("apply_fused_kernel", cfg) is None
+            assert bench.kernel_traffic(kernel, {**cfg, key: other}, str(cur)) is None
+    assert bench.kernel_traffic("apply_fused_kernel", cfg, str(cur)) is None
+    stale = json.loads(cur.read_text())
+    for ent in stale["kernels"].values():
+        ent["source_sha256"] = "0" * 64
+    old = tmp_path / "stale.json"
+    old.write_text(json.dumps(stale))
+    for kernel in stale["kernels"]:
+        assert bench.kernel_traffic(kernel, cfg, str(old)) is None

@@ -29,7 +29,7 @@ namespace {
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
-constexpr int kKvThreadsFused = 192 + 32 * kKsumGroups / 2;  // + warps 6..11: the producer-step transform
+constexpr int kKvThreadsFused = 192 + 32 * kKsumGroups / 2;  // + warps 6..13: the producer-step transform
 constexpr int kKvTransformThreads = kKvThreadsFused - 192;
 // Tiles per tensor-core sub-chunk before its sum is promoted into FP32 registers: 4 (256
 // tokens) in the 'high' tier, 1 (64 tokens) in the 'lossless' tier.
@@ -48,6 +48,11 @@ struct KvLayout {
     static constexpr uint32_t stage_bytes = a_bytes + b_bytes + (FUSED ? 2 * tab_bytes : 0);
     static constexpr uint32_t bar_offset = stages * stage_bytes;
     static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;  // + barriers + alignment slack
+    // TMEM: two 128-column accumulators; the fused kernel keeps the segment's running sum in
+    // a third region (columns 256..383) instead of registers, which leaves the registers to
+    // its transform warps.
+    static constexpr uint32_t tmem_cols = FUSED ? 512 : 256;
+    static constexpr uint32_t sum_col = 256;
 };
 
 // Tiles [t_s, t_e) of the CTA's chunk, clipped to the launch's head range.
@@ -115,7 +120,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), 256);
+        tmem_alloc(smem_u32(tmem_holder), L::tmem_cols);
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -299,17 +304,22 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         }
     } else if (!FUSED || warp < 6) {
         // ---------------- epilogue: TMEM lanes 32q..32q+31 = rows i of the partial KV.
-        // Thread i keeps its row of the segment's running sum in registers.
+        // Thread i keeps its row of the segment's running sum in registers (plain kernel) or in
+        // TMEM columns sum_col.. (fused kernel); either way each finished sub-chunk is added into
+        // it with one FP32 add per element, in sub-chunk order.
         const int q = warp & 3;
         const int i = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         uint32_t sub = 0;
         bool ok = true;
         for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
             const int h = static_cast<int>(t / tph);
             const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
-            float acc[64 * NBOX];
+            float acc[FUSED ? 1 : 64 * NBOX];
+            if constexpr (!FUSED) {
 #pragma unroll
-            for (int c = 0; c < 64 * NBOX; ++c) acc[c] = 0.f;
+                for (int c = 0; c < 64 * NBOX; ++c) acc[c] = 0.f;
+            }
             for (int64_t k0 = t; k0 < seg_end; k0 += PROMOTE, ++sub) {
                 const uint32_t buf = sub & 1u;
                 if (!mbar_wait(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status)) {
@@ -317,32 +327,56 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
+                const uint32_t taddr = tmem + lane_base + buf * 128u;
 #pragma unroll
                 for (int c = 0; c < 4 * NBOX; ++c) {
                     if (16 * c < head_dim) {
                         uint32_t r[16];
                         tmem_ld16_sync(taddr + 16u * c, r);
+                        if constexpr (FUSED) {
+                            const uint32_t saddr = tmem + lane_base + L::sum_col + 16u * c;
+                            uint32_t sv[16];
+                            if (k0 == t) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) acc[16 * c + e] += __uint_as_float(r[e]);
+                                for (int e = 0; e < 16; ++e) sv[e] = __float_as_uint(__fadd_rn(0.f, __uint_as_float(r[e])));
+                            } else {
+                                tmem_ld16_sync(saddr, sv);
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    sv[e] = __float_as_uint(__fadd_rn(__uint_as_float(sv[e]), __uint_as_float(r[e])));
+                            }
+                            tmem_st16(saddr, sv);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) acc[16 * c + e] += __uint_as_float(r[e]);
+                        }
                     }
                 }
+                if constexpr (FUSED) tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acc_empty0 + 8u * buf);
             }
             if (!ok) break;
-            if (i < head_dim) {
-                const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
-                float* dst = partial + (slot * head_dim + i) * head_dim;
+            const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
+            float* dst = partial + (slot * head_dim + i) * head_dim;
 #pragma unroll
-                for (int c = 0; c < 4 * NBOX; ++c) {
-                    if (16 * c < head_dim) {
+            for (int c = 0; c < 4 * NBOX; ++c) {
+                if (16 * c < head_dim) {
+                    float v[16];
+                    if constexpr (FUSED) {
+                        uint32_t sv[16];
+                        tmem_ld16_sync(tmem + lane_base + L::sum_col + 16u * c, sv);  // warp-collective
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(sv[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = acc[16 * c + e];
+                    }
+                    if (i < head_dim) {
                         float4* o = reinterpret_cast<float4*>(dst + 16 * c);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            o[e] = make_float4(acc[16 * c + 4 * e], acc[16 * c + 4 * e + 1], acc[16 * c + 4 * e + 2],
-                                               acc[16 * c + 4 * e + 3]);
+                        for (int e = 0; e < 4; ++e) o[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     }
                 }
             }
@@ -354,7 +388,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, L::tmem_cols);
     }
 }
 

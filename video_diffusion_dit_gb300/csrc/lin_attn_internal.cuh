@@ -137,7 +137,7 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 //   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
 // Row groups of the fused KV kernel's transform (one column-sum partial each).
 #ifndef LA_KSUM_GROUPS
-#define LA_KSUM_GROUPS 12
+#define LA_KSUM_GROUPS 16
 #endif
 constexpr int kKsumGroups = LA_KSUM_GROUPS;
 struct ProducerArgs {
