@@ -364,9 +364,12 @@ def run_ours(args, w, world, rank, local, dist):
     ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode, stream=stream)
     barrier(dist, dev)
     t0 = time.perf_counter()
+    e2e_step_ms = []
     for _ in range(e2e_steps):
+        t1 = time.perf_counter()
         ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
                          stream=stream)
+        e2e_step_ms.append((time.perf_counter() - t1) * 1e3)
     e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev) / e2e_steps
     h2d = 3 * H * N * D * 2 + H * N * 4
     d2h = H * N * D * out_bytes
@@ -407,7 +410,9 @@ def run_ours(args, w, world, rank, local, dist):
                          "traffic": kernel_traffic(kernel_names[dom], traffic_config),
                          "algorithmic_bytes": nbytes[dom]},
             "e2e": {"value": world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps,
+                    "step_ms": {"min": min(e2e_step_ms), "p50": float(np.median(e2e_step_ms)), "max": max(e2e_step_ms)},
+                    "note": "bound by the host-device link; varies with other traffic on the host"},
             "gpu_launches": 3 * args.steps,
             "stage_ms_note": "per-kernel means from a second pass of the same steps with events around each kernel",
             "clocks": clk,
