@@ -48,6 +48,12 @@ constexpr int kFRowGroups = kFTransformThreads / 16;  // a transform thread take
 constexpr int kFTabSubs = LA_FUSED_TAB_SUBS;        // table slots per tile
 constexpr int kFTabSlots = 3 * kFTabSubs / 2;       // table ring: 1.5 tiles of rows
 constexpr uint32_t kFOutBufs = 1;                   // staging buffers per epilogue warp
+// Reciprocal-denominator buffers between the transform and the epilogue.  A buffer is
+// written by the transform of tile i and freed by the epilogue of tile i after the MMA, so
+// the ring must span the whole transform -> MMA -> epilogue chain (~9000 cycles at
+// D = 112, ~2 tile periods): with 2 buffers that chain, not any one stage, set the pace;
+// 3 cover it (4 do not fit beside the D = 128 layout).
+constexpr uint32_t kFDenBufs = 3;
 constexpr int kFTabRows = kApplyTile / kFTabSubs;   // tokens per table slot
 constexpr uint32_t kFQAtom = kApplyTile * 128;      // 128 token rows x 128 bytes
 constexpr uint32_t kFBoxBytes = 32 * 128;           // staging box: 32 tokens x 128 bytes
@@ -63,11 +69,13 @@ __host__ __device__ constexpr uint32_t fused_tab_slot_bytes(int head_dim) {
 __host__ __device__ constexpr uint32_t fused_smem_bytes(int head_dim) {
     return fused_stages(head_dim_atoms(head_dim)) * head_dim_atoms(head_dim) * kFQAtom +
            kFTabSlots * fused_tab_slot_bytes(head_dim) + kFEpiWarps * kFOutBufs * kFBoxBytes + kFBarBytes +
-           2 * kApplyTile * 4 + 1024;
+           kFDenBufs * kApplyTile * 4 + 1024;
 }
 static_assert(fused_smem_bytes(128) <= kFSmemLimit && fused_smem_bytes(64) <= kFSmemLimit,
               "fused apply layout exceeds shared memory");
 static_assert(kFImgCol + 3 * 64 <= 512, "accumulators and image exceed TMEM");
+static_assert((3 * fused_stages(1) + 4 + 2 * kFDenBufs + 2 * kFTabSlots + 3) * 8 <= kFBarBytes - 64,
+              "barriers overlap the TMEM address slot");
 static_assert(kFTabRows % (kFXfWarps * 32 / 16) == 0, "a table slot must hold whole row groups");
 
 template <int NBOX, bool OUT_BF16>
@@ -92,16 +100,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t q_ready0 = q_empty0 + 8u * kStages;         // [stages] transformed
     const uint32_t acc_full0 = q_ready0 + 8u * kStages;        // [2]
     const uint32_t acc_empty0 = acc_full0 + 16u;               // [2]
-    const uint32_t den_full0 = acc_empty0 + 16u;               // [2] reciprocal denominators written
-    const uint32_t den_empty0 = den_full0 + 16u;               // [2] ... and read
-    const uint32_t tab_full0 = den_empty0 + 16u;               // [kFTabSlots]
+    const uint32_t den_full0 = acc_empty0 + 16u;               // [kFDenBufs] reciprocal denominators written
+    const uint32_t den_empty0 = den_full0 + 8u * kFDenBufs;    // [kFDenBufs] ... and read
+    const uint32_t tab_full0 = den_empty0 + 8u * kFDenBufs;    // [kFTabSlots]
     const uint32_t tab_empty0 = tab_full0 + 8u * kFTabSlots;   // [kFTabSlots]
     const uint32_t b_full = tab_empty0 + 8u * kFTabSlots;      // the head's image is in TMEM
     const uint32_t b_empty = b_full + 8u;                      // the old image's MMAs are done
     const uint32_t drain_bar = b_empty + 8u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + kFBarBytes - 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + bar_off + kFBarBytes - 56);
-    float* rcp_s = reinterpret_cast<float*>(base_ptr + bar_off + kFBarBytes);  // [2][kApplyTile]
+    float* rcp_s = reinterpret_cast<float*>(base_ptr + bar_off + kFBarBytes);  // [kFDenBufs][kApplyTile]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -129,6 +137,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
             mbar_init(acc_empty0 + 8u * b, kFEpiWarps);
+        }
+        for (uint32_t b = 0; b < kFDenBufs; ++b) {
             mbar_init(den_full0 + 8u * b, kFTransformThreads);
             mbar_init(den_empty0 + 8u * b, kFEpiWarps);
         }
@@ -276,9 +286,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 }
             }
             const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
-            const uint32_t buf = lt & 1u;
+            const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
             if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
-            if (!mbar_wait(den_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+            if (!mbar_wait(den_empty0 + 8u * db, dph ^ 1u, abort_flag, status)) break;
             uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kFQAtom;
             bool ok = true;
 #pragma unroll
@@ -314,14 +324,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     part += __shfl_xor_sync(0xffffffffu, part, 4);
                     part += __shfl_xor_sync(0xffffffffu, part, 2);
                     part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    if (c == 0) rcp_s[buf * kApplyTile + r] = __frcp_rn(part + kDenEps);
+                    if (c == 0) rcp_s[db * kApplyTile + r] = __frcp_rn(part + kDenEps);
                 }
                 mbar_arrive(tab_empty0 + 8u * slot);
             }
             if (!ok) break;
             fence_proxy_async_smem();
             mbar_arrive(q_ready0 + 8u * st);
-            mbar_arrive(den_full0 + 8u * buf);
+            mbar_arrive(den_full0 + 8u * db);
         }
     } else {
         // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes = output features
@@ -380,10 +390,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (lane == 0) mbar_arrive(b_full);
             }
             const uint32_t buf = lt & 1u;
-            if (!(ok = mbar_wait(den_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status))) break;
+            const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
+            if (!(ok = mbar_wait(den_full0 + 8u * db, dph, abort_flag, status))) break;
             if (!(ok = mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status))) break;
             tc_fence_after();
-            const float* rcp_t = rcp_s + buf * kApplyTile;
+            const float* rcp_t = rcp_s + db * kApplyTile;
             for (int g = 2 * e; g < 2 * e + 2 && n0 + 32 * g < n_tokens; ++g) {
                 uint32_t r[32];
                 tmem_ld32_sync(tmem + lane_base + buf * kFAccCols + 32u * g, r);
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 ++nstore;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(den_empty0 + 8u * buf);
+            if (lane == 0) mbar_arrive(den_empty0 + 8u * db);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty0 + 8u * buf);
