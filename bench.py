@@ -222,9 +222,20 @@ def cpu_baseline(layer_np, H, N, budget_s=12.0):
     hs = int(max(1, min(H, budget_s // max(t1, 1e-3))))
     t = oracle_sample_time(layer_np, hs) if hs > 1 else t1
     per_layer = t * H / hs
+    # The same oracle on one core: one head x the first min(N, 32760) tokens (the 480p layer's
+    # length), scaled to the layer (the work is linear in heads x tokens).
+    n1 = min(N, 32760)
+    oracle.set_num_threads(1)
+    try:
+        t_one = oracle_slice_time(layer_np, 1, n1)
+    finally:
+        oracle.set_num_threads(cores)
+    per_layer_one = t_one * H * N / n1
     return {"value": N / per_layer, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{hs} of {H} heads, all {N} tokens (KV + apply, FP64); time scaled x{H / hs:.2f} "
-                      f"to one layer call ({t:.2f} s measured)"}
+                      f"to one layer call ({t:.2f} s measured)",
+            "one_core": {"value": N / per_layer_one, "unit": UNIT,
+                         "sample": f"1 head x {n1} tokens on one thread ({t_one:.2f} s), scaled to the layer"}}
 
 
 def layer_to_numpy(layer):
