@@ -51,6 +51,40 @@ def test_header_compiles_as_c():
     assert r.returncode == 0, r.stderr
 
 
+def test_plain_c_program_links_and_calls_the_library(la, tmp_path):
+    # The boundary from C itself (no ctypes): link against the library, call the entry
+    # points that need no GPU, and check what they answer.
+    src = tmp_path / "abi_client.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "lin_attn.h"
+int main(void) {
+    if (lin_attn_version() != LIN_ATTN_VERSION) return 10;
+    if (strcmp(lin_attn_error_string(LIN_ATTN_OK), lin_attn_error_string(99)) == 0) return 11;
+    lin_attn_ctx *ctx = (lin_attn_ctx *)0x1;
+    if (lin_attn_create(&ctx, 0, 1000, 112, 0) != LIN_ATTN_ERR_INVALID_ARG) return 12;
+    if (ctx != NULL) return 13;
+    if (lin_attn_create(&ctx, 20, 1000, 100, 0) != LIN_ATTN_ERR_UNSUPPORTED) return 14;
+    if (strstr(lin_attn_last_error(), "head_dim") == NULL) return 15;
+    int chunks = 0, segs = 0;
+    if (lin_attn_kv_plan(20, 180320, LIN_ATTN_MODE_HIGH, &chunks, &segs) != LIN_ATTN_OK) return 16;
+    if (chunks != 140 || segs != 7) return 17;
+    if (lin_attn_kv_plan(0, 10, LIN_ATTN_MODE_HIGH, &chunks, &segs) != LIN_ATTN_ERR_INVALID_ARG) return 18;
+    if (lin_attn_destroy(NULL) != LIN_ATTN_OK) return 19;
+    puts("ok");
+    return 0;
+}
+""")
+    exe = tmp_path / "abi_client"
+    libdir = os.path.dirname(LIB)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        "-L", libdir, "-llin_attn", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+
+
 def test_version_and_error_strings(la):
     assert la.lib.lin_attn_version() == 100
     for code in range(7):
