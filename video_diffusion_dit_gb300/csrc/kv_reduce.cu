@@ -23,7 +23,8 @@ namespace {
 
 // ============================================================================ tensor cores
 // Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma, warps 2..5 drain the
-// TMEM accumulator.  Per stage, one 64-token tile of K and of V is loaded with 128-byte
+// TMEM accumulator; the fused-producer instantiation adds warps 6..13, which turn each
+// loaded K tile into relu(K) rotated (in place) and sum the columns of relu(K).  Per stage, one 64-token tile of K and of V is loaded with 128-byte
 // swizzle as [token][64 head-dim columns] boxes - exactly the MN-major canonical layout of
 // the MMA operands A = K^T (M = head-dim row i) and B = V (N = head-dim column j), with
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             }
             if (!ok) break;
             // This row group's column sums of the segment: [h][slot][rg][column] (the
-            // reduction adds the 8 row groups in order, then the segments).
+            // reduction adds the row groups in order, then the segments).
             if (live) {
                 const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
                 double* dst = pa.ksum_partial + (slot * kKsumGroups + rg) * head_dim + 8 * c;
