@@ -161,3 +161,36 @@ def test_binding_rejects_wrong_tensors_without_gpu(la):
         la._mode("fast")
     with pytest.raises(TypeError):
         la._out_code(torch.float16)
+
+
+def test_binding_rejects_wrong_fused_and_anchor_arguments_without_gpu(la):
+    import torch
+    # The fused-producer and anchor calls check their tensors before the library is reached.
+    obj = la.LinAttn.__new__(la.LinAttn)
+    obj.heads, obj.head_dim, obj.max_tokens = 2, 32, 64
+    obj.device = torch.device("cpu")
+    obj._h = None
+    q = torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16)
+    cos = torch.zeros(8, 16)
+    with pytest.raises(ValueError):  # float32 activations
+        obj.forward_fused(q.float(), q, q, cos, cos)
+    with pytest.raises(ValueError):  # shapes differ
+        obj.forward_fused(q, q[:, :, :4].contiguous(), q, cos, cos)
+    with pytest.raises(ValueError):  # unknown layout
+        obj.forward_fused(q, q, q, cos, cos, layout="bnhd")
+    with pytest.raises(ValueError):  # table rows must match N
+        obj.forward_fused(q, q, q, torch.zeros(9, 16), cos)
+    with pytest.raises(ValueError):  # tables must be float32
+        obj.forward_fused(q, q, q, cos, cos.double())
+    with pytest.raises(ValueError):  # token-major input read with the context's H = 2: N = 2, H = 8
+        obj.forward_fused(q, q, q, cos, cos, layout="nhd")
+    with pytest.raises(ValueError):  # out of the wrong size
+        obj.forward_fused(q, q, q, cos, cos, out=torch.zeros(3))
+    with pytest.raises(ValueError):  # anchor: head count of another context
+        obj.anchor_forward(torch.zeros(1, 3, 8, 32, dtype=torch.bfloat16), *(torch.zeros(1, 3, 8, 32,
+                                                                                       dtype=torch.bfloat16),) * 2)
+    with pytest.raises(ValueError):  # anchor: non-contiguous
+        qt = q.transpose(2, 3).contiguous().transpose(2, 3)
+        obj.anchor_forward(qt, q, q)
+    with pytest.raises(ValueError):  # anchor: out of the wrong shape
+        obj.anchor_forward(q, q, q, out=torch.zeros(1, 2, 8, 16, dtype=torch.bfloat16))
