@@ -112,6 +112,27 @@ def test_calls_on_null_context_are_rejected(la):
     assert la.lib.lin_attn_device_status(None, None) == la.ERR_INVALID_ARG
     assert la.lib.lin_attn_set_stage_events(None, None, 0) == la.ERR_INVALID_ARG
     assert la.lib.lin_attn_destroy(None) == la.OK
+    assert la.lib.lin_attn_forward_layout(None, p, p, p, p, p, 0, 10, 0, 0, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_forward_fused(None, p, p, p, p, p, p, 0, 10, 0, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_forward_fused_layout(None, p, p, p, p, p, p, 0, 10, 0, 0, None) == la.ERR_INVALID_ARG
+    assert la.lib.lin_attn_anchor_forward(None, p, p, p, p, 0, 10, 0.0, None) == la.ERR_INVALID_ARG
+    # Checks that come before any CUDA call, whatever the context.
+    assert la.lib.lin_attn_forward_fused_layout(None, p, p, p, p, p, p, 0, 10, 0, 7, None) == la.ERR_INVALID_ARG
+    assert b"layout" in la.lib.lin_attn_last_error()
+    assert la.lib.lin_attn_forward_fused_layout(None, p, p, p, None, p, p, 0, 10, 0, 0, None) == la.ERR_INVALID_ARG
+    assert b"rotation table" in la.lib.lin_attn_last_error()
+
+
+def test_noalloc_entry_checks_arguments_before_any_cuda_call(la):
+    p = ctypes.c_void_p(16)
+    f = la.lib.lin_attn_forward_noalloc
+    assert f(None, p, p, p, p, 0, 20, 1000, 112, 0, None) == la.ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 0, 0, 1000, 112, 0, None) == la.ERR_INVALID_ARG       # heads
+    assert f(p, p, p, p, p, 0, 20, 0, 112, 0, None) == la.ERR_INVALID_ARG         # n_tokens
+    assert f(p, p, p, p, p, 0, 20, 1000, 100, 0, None) == la.ERR_UNSUPPORTED      # head_dim
+    assert f(p, p, p, p, p, 0, 20, 1000, 112, 5, None) == la.ERR_INVALID_ARG      # mode
+    assert f(p, p, p, p, p, 9, 20, 1000, 112, 0, None) == la.ERR_INVALID_ARG      # out dtype
+    assert b"out_dtype" in la.lib.lin_attn_last_error()
 
 
 def test_kv_plan_depends_on_shape_and_tier_only(la):
