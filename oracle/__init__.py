@@ -60,6 +60,8 @@ def _bind(lib):
     lib.oracle_kv.restype = ctypes.c_int
     lib.oracle_apply_rows.argtypes = [i64, i64, i64, p, p, p, i64, p, p]
     lib.oracle_apply_rows.restype = ctypes.c_int
+    lib.oracle_apply_rows_f64den.argtypes = [i64, i64, i64, p, p, p, i64, p, p]
+    lib.oracle_apply_rows_f64den.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [i64, i64, i64, p, p, p, p, p]
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_bf16_decode.argtypes = [i64, p, p]
@@ -156,38 +158,29 @@ def kv(k_bits, v_bits, lib=None) -> np.ndarray:
 
 def apply_rows(q_bits, kv_f64, den, rows=None, lib=None) -> np.ndarray:
     """Normalised second GEMM for the given flat rows (h*N + n); [len(rows), D].
-    den: FP32 denominators (the layer's input) or FP64 ones (from `producer`)."""
+    den: FP32 denominators (the layer's input) or FP64 ones (from `producer`); each is
+    handled by its own C routine (oracle_apply_rows / oracle_apply_rows_f64den)."""
     q_bits = _u16(q_bits)
     H, N, D = _shape3(q_bits)
     kv_f64 = np.ascontiguousarray(kv_f64, dtype=np.float64)
-    den = np.ascontiguousarray(den).reshape(H, N)
-    if den.dtype == np.float64:
-        return _apply_rows_f64den(q_bits, kv_f64, den, rows, lib)
-    den = _f32(den)
     if kv_f64.shape != (H, D, D):
         raise ValueError("kv shape mismatch")
+    den = np.ascontiguousarray(den).reshape(H, N)
+    if den.dtype == np.float64:
+        fn = (lib or load()).oracle_apply_rows_f64den
+    else:
+        den = _f32(den)
+        fn = (lib or load()).oracle_apply_rows
     if rows is None:
         n_rows, rows_ptr = H * N, None
     else:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         n_rows, rows_ptr = rows.size, _ptr(rows)
     out = np.empty((n_rows, D), np.float64)
-    rc = (lib or load()).oracle_apply_rows(H, N, D, _ptr(q_bits), _ptr(kv_f64), _ptr(den),
-                                           n_rows, rows_ptr, _ptr(out))
+    rc = fn(H, N, D, _ptr(q_bits), _ptr(kv_f64), _ptr(den), n_rows, rows_ptr, _ptr(out))
     if rc:
-        raise RuntimeError(f"oracle_apply_rows failed ({rc})")
+        raise RuntimeError(f"oracle apply failed ({rc})")
     return out
-
-
-def _apply_rows_f64den(q_bits, kv_f64, den64, rows, lib):
-    # Same loops as oracle_apply_rows with the division by an FP64 denominator: run the
-    # FP32-denominator routine with den = 1 and divide here (both exact in FP64 up to the
-    # one rounding of each quotient).
-    H, N, D = q_bits.shape
-    ones = np.ones((H, N), np.float32)
-    num = apply_rows(q_bits, kv_f64, ones, rows, lib)
-    flat = np.arange(H * N) if rows is None else np.asarray(rows, np.int64)
-    return num / den64.reshape(-1)[flat][:, None]
 
 
 def forward(q_bits, k_bits, v_bits, den, lib=None) -> np.ndarray:

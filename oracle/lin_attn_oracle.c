@@ -227,6 +227,43 @@ int oracle_apply_rows(int64_t H, int64_t N, int64_t D, const uint16_t *q, const 
 }
 
 /*
+ * The same second GEMM and normalisation with FP64 denominators, as the producer step
+ * forms them (oracle_producer writes den in FP64; page 1, snippet `sana_video.py`, divides
+ * the second product by the normaliser built from the un-rotated ReLU'd Q and K):
+ *   out[r][j] = (sum over i = 0..D-1 (ascending) of Q[row_r][i] * KV[h_r][i][j]) / den64[row_r]
+ * Arguments as oracle_apply_rows, except den64: FP64 [H][N].
+ */
+int oracle_apply_rows_f64den(int64_t H, int64_t N, int64_t D, const uint16_t *q, const double *kv,
+                             const double *den64, int64_t n_rows, const int64_t *rows, double *out)
+{
+    if (H < 0 || N < 0 || D < 1 || !q || !kv || !den64 || !out || n_rows < 0)
+        return 1;
+    if (!rows && n_rows != H * N)
+        return 1;
+    int bad = 0;
+    int64_t r;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (r = 0; r < n_rows; ++r) {
+        const int64_t flat = rows ? rows[r] : r;
+        if (flat < 0 || flat >= H * N) {
+            bad |= 1;
+            continue;
+        }
+        const int64_t h = flat / N;
+        const uint16_t *qrow = q + flat * D;
+        const double *kvh = kv + h * D * D;
+        const double dd = den64[flat];
+        for (int64_t j = 0; j < D; ++j) {
+            double s = 0.0;
+            for (int64_t i = 0; i < D; ++i)
+                s += bf16_to_f64(qrow[i]) * kvh[i * D + j];
+            out[r * D + j] = s / dd;
+        }
+    }
+    return bad;
+}
+
+/*
  * Softmax attention for selected rows: rows[r] = h*N + n (rows == NULL: all H*N in order).
  * q, k, v: BF16 bits [H][N][D]; out: FP64 [n_rows][D].  Scores, weights and sums in FP64,
  * keys m ascending.

@@ -96,8 +96,21 @@ def producer_pins_hold(lib) -> bool:
     return bool(np.array_equal(oracle.f32_to_bf16(vals, lib=lib), bf16_bits(torch.from_numpy(vals).to(torch.bfloat16))))
 
 
+# Slips in the second GEMM with FP64 denominators (the fused path's reference).
+F64DEN_MUTANTS = {
+    "f64den_multiply": ("out[r * D + j] = s / dd;", "out[r * D + j] = s * dd;"),
+    "f64den_sample_index": ("const double dd = den64[flat];", "const double dd = den64[r];"),
+    "f64den_rounded_to_f32": ("const double dd = den64[flat];", "const double dd = (double)(float)den64[flat];"),
+    "f64den_den_of_wrong_head": ("const double dd = den64[flat];", "const double dd = den64[flat % N];"),
+    "f64den_last_dim_dropped": ("for (int64_t i = 0; i < D; ++i)\n                s += bf16_to_f64(qrow[i]) * kvh[i * D + j];\n            out[r * D + j] = s / dd;",
+                                "for (int64_t i = 0; i < D - 1; ++i)\n                s += bf16_to_f64(qrow[i]) * kvh[i * D + j];\n            out[r * D + j] = s / dd;"),
+}
+
+
 def test_unmodified_oracle_passes(oracle_lib):
+    from test_oracle_f64den_pins import f64den_pins_hold
     assert pins_hold(oracle_lib)
+    assert f64den_pins_hold(oracle_lib)
     assert producer_pins_hold(oracle_lib)
     assert softmax_pins_hold(oracle_lib)
 
@@ -130,3 +143,14 @@ def test_mutant_is_caught(tmp_path, name):
     src.write_text(SRC.replace(old, new))
     lib = oracle.load(lib_path=str(tmp_path / f"lib{name}.so"), src=str(src))
     assert not pins_hold(lib), f"pins missed the planted slip {name}"
+
+
+@pytest.mark.parametrize("name", sorted(F64DEN_MUTANTS))
+def test_f64den_mutant_is_caught(tmp_path, name):
+    from test_oracle_f64den_pins import f64den_pins_hold
+    old, new = F64DEN_MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / f"{name}.c"
+    src.write_text(SRC.replace(old, new))
+    lib = oracle.load(lib_path=str(tmp_path / f"lib{name}.so"), src=str(src))
+    assert not f64den_pins_hold(lib), f"pins missed the planted slip {name}"

@@ -27,6 +27,8 @@ for H, N, D in ((1, 1, 2), (2, 37, 16), (3, 5, 112)):
     kv = oracle.kv(k, v, lib=lib)
     ends = np.array(sorted({0, H * N - 1}), np.int64)
     oracle.apply_rows(q, kv, den, rows=ends, lib=lib)
+    oracle.apply_rows(q, kv, den.astype(np.float64) + 2.0 ** -40, rows=ends, lib=lib)
+    oracle.apply_rows(q, kv, den.astype(np.float64), lib=lib)
     cos = rng.random((N, D // 2)).astype(np.float32)
     sin = rng.random((N, D // 2)).astype(np.float32)
     oracle.producer(q, k, cos, sin, lib=lib)
