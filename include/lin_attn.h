@@ -203,6 +203,19 @@ int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
 int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *max_segments);
 
 /*
+ * Test hook: how long a kernel of this context's later calls waits on one of its own
+ * barriers before it gives up, in nanoseconds (0 restores the default of 2 s; larger values
+ * are LIN_ATTN_ERR_INVALID_ARG).  A kernel that gives up winds down cleanly - it lets its
+ * copies and tensor-core operations in flight land, frees its tensor memory and exits -
+ * and records LIN_ATTN_ERR_TIMEOUT for lin_attn_device_status; that call's output is then
+ * incomplete.  Limits below 1 ms are checked with non-blocking barrier probes, so a wait
+ * that is not already over when it starts gives up within about the limit.  Used to show
+ * that the bounded waits report instead of hanging; calls made with the default limit are
+ * unaffected.
+ */
+int lin_attn_set_wait_limit(lin_attn_ctx *ctx, uint64_t limit_ns);
+
+/*
  * Timing hook.  Arms `n_events` (must be 4) CUDA events (created with timing enabled)
  * for the NEXT lin_attn_forward call only: events[0] is recorded before the KV partial
  * kernel, events[1] after it, events[2] after the reduction, events[3] after apply.
@@ -223,13 +236,18 @@ int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *event
  * thread's current device.  Its scratch is one fixed 48 MiB array compiled into the
  * library, which every GPU that loads the library holds until the process exits; the
  * call itself makes no cudaMalloc, cudaFree or other allocating call.
- *   - A shape whose scratch (heads x partial slots x head_dim^2 FP32 partial sums, plus
- *     the reduced KV and its image; see lin_attn_kv_plan) does not fit in 48 MiB is
- *     rejected with LIN_ATTN_ERR_INVALID_ARG.  The 720p/193-frame layer (20 x 180320 x 112)
- *     needs ~12 MiB in the 'high' tier and ~34 MiB in the 'lossless' tier.
- *   - The first call on a device resolves the array's device address once
- *     (cudaGetSymbolAddress, with that device current): make that first call before any
- *     stream capture.
+ *   - The scratch a shape needs does not depend on the tier.  With k = the partial slots
+ *     per head of lin_attn_kv_plan (max_segments) and every term rounded up to 256 bytes:
+ *       heads * k * head_dim^2 * 4          (FP32 partial sums)
+ *     + heads * head_dim^2 * 4              (reduced KV)
+ *     + heads * 3 * ceil(head_dim / 64) * head_dim * 128   (the KV image)
+ *     + 256                                 (status word)
+ *     A shape that needs more than 48 MiB is rejected with LIN_ATTN_ERR_INVALID_ARG.  The
+ *     720p/193-frame layer (20 x 180320 x 112, k = 7) needs ~9.3 MiB; at head_dim 128 and
+ *     1 slot per head (heads >= 153) the limit is 219 heads.
+ *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress,
+ *     with that device current) and keeps it; a failed attempt is not kept, so the next
+ *     call retries.  Make that first call before any stream capture.
  *   - Every call uses the same array and it keeps the previous call's contents; each call
  *     clears what has to start at zero.  Calls that overlap on the GPU (from several
  *     streams or host threads) race on the array and corrupt each other's results, so

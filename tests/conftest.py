@@ -57,3 +57,18 @@ def rel_l2(a, b) -> float:
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+def whole_and_head_rel_l2(got, ref):
+    """Relative L2 over the whole [H, N, D] result and the largest per-head relative L2.
+    got: torch tensor (any device, any float dtype, H*N*D elements in head-major order);
+    ref: FP64 numpy array or tensor of the same elements.  Computed on got's device."""
+    r = torch.as_tensor(ref).to(got.device, torch.float64)
+    H = r.shape[0]
+    g = got.reshape(r.shape).to(torch.float64)
+    d = (g - r).reshape(H, -1)
+    r = r.reshape(H, -1)
+    rn = torch.linalg.vector_norm(r, dim=1)
+    whole = (torch.linalg.vector_norm(d) / torch.linalg.vector_norm(r)).item()
+    per_head = (torch.linalg.vector_norm(d, dim=1) / torch.where(rn > 0, rn, torch.ones_like(rn))).max().item()
+    return whole, per_head

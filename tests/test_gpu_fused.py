@@ -3,12 +3,11 @@ normaliser computed inside the kernels from the pre-activation q, k and FP32 rot
 tables.  Held to the FP64 oracle (its producer step, then the layer) with the same
 tolerances as the plain call; and because the rotation is defined bit for bit, the reduced
 KV must equal, bitwise, the KV the plain call forms from the generator's Q_rot/K_rot."""
-import numpy as np
 import pytest
 import torch
 
 import oracle
-from conftest import bf16_bits, rel_l2
+from conftest import bf16_bits, rel_l2, whole_and_head_rel_l2
 from video_diffusion_dit_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -89,21 +88,31 @@ def test_fused_480p(la, dev):
     check(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid, dtypes=(torch.float32,))
 
 
-def test_fused_720p_sampled(la, dev):
+def test_fused_720p_whole_tensor(la, dev):
+    """The full 720p layer through the fused call, every output element against the oracle,
+    both tiers and output types; the model's token-major layout gives the same bits; repeated
+    calls are bitwise identical."""
     w = synth.WORKLOADS["720p_193f"]
     H, N, D = w.heads, w.tokens, w.head_dim
     layer = synth.make_workload(w, device=dev, producer_inputs=True)
-    rows = np.unique(np.concatenate([np.random.default_rng(2).choice(H * N, 2048, replace=False),
-                                     [0, N - 1, N, H * N - 1]])).astype(np.int64)
-    ref, kv_ref = oracle_fused(layer, rows)
+    ref, kv_ref = oracle_fused(layer)
+    ref = torch.from_numpy(ref.reshape(H, N, D)).to(dev)
+    nhd = {key: layer[key].permute(0, 2, 1, 3).contiguous() for key in ("q", "k", "v")}
+    tabs = (layer["rope_cos"], layer["rope_sin"])
     with la.LinAttn(H, N, D, dev) as ctx:
-        out = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"])
-        assert ctx.device_status() == 0
-        got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
-        assert rel_l2(got, ref) <= TOL[torch.float32]
-        assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= 1e-6
-        again = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"]).clone()
-        third = ctx.forward_fused(layer["q"], layer["k"], layer["v"], layer["rope_cos"], layer["rope_sin"])
+        for mode in ("high", "lossless"):
+            for dt in (torch.float32, torch.bfloat16):
+                out = ctx.forward_fused(layer["q"], layer["k"], layer["v"], *tabs, out_dtype=dt, mode=mode)
+                assert ctx.device_status() == 0
+                whole, head = whole_and_head_rel_l2(out, ref)
+                assert whole <= TOL[dt] and head <= TOL[dt], f"fused 720p {mode} {dt}: {whole:.3e} / {head:.3e}"
+                assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= 1e-6
+                tm = ctx.forward_fused(nhd["q"], nhd["k"], nhd["v"], *tabs, out_dtype=dt, mode=mode, layout="nhd")
+                assert ctx.device_status() == 0
+                assert torch.equal(tm.reshape(1, N, H, D).permute(0, 2, 1, 3), out), (mode, dt)
+                del out, tm
+        again = ctx.forward_fused(layer["q"], layer["k"], layer["v"], *tabs).clone()
+        third = ctx.forward_fused(layer["q"], layer["k"], layer["v"], *tabs)
         assert torch.equal(again, third)
 
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from conftest import rel_l2
+from conftest import rel_l2, whole_and_head_rel_l2
 from video_diffusion_dit_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +32,11 @@ def dev():
 
 def to_dev(layer, dev):
     return {k: t.to(dev) for k, t in layer.items()}
+
+
+def to_token_major(t):
+    """[1, H, N, D] -> contiguous [1, N, H, D]."""
+    return t.permute(0, 2, 1, 3).contiguous()
 
 
 def run(ctx, g, mode, dt):
@@ -97,58 +102,61 @@ def test_480p_full_all_modes(la, dev):
     check_full(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid)
 
 
-def sampled_rows(H, N, count, seed):
-    rng = np.random.default_rng(seed)
-    rows = rng.choice(H * N, size=count, replace=False)
-    edges = [0, N - 1, N, H * N - 1, (H - 1) * N, 127, 128, N - 128, N - 129]
-    return np.unique(np.concatenate([rows, [r for r in edges if 0 <= r < H * N]])).astype(np.int64)
+def check_whole(out, ref, dt, what):
+    """Whole-tensor and per-head relative L2 of a full-size result against the oracle."""
+    whole, head = whole_and_head_rel_l2(out, ref)
+    assert whole <= TOL[dt] and head <= TOL[dt], f"{what}: rel-L2 {whole:.3e}, worst head {head:.3e}"
 
 
 @pytest.mark.parametrize("name", ["720p_193f", "720p_193f_d64"])
-def test_full_size_sampled(la, dev, name):
-    """Full-size layer in the bench's launch configuration: KV checked whole, output on
-    sampled rows (the first/last rows of heads, tile edges and random rows)."""
+def test_full_size_whole_tensor(la, dev, name):
+    """Full-size layer in the bench's launch configuration, every output element against the
+    oracle, both tiers and output types; the token-major call on the same data gives the
+    same bits as the head-major call."""
     w = synth.WORKLOADS[name]
     H, N, D = w.heads, w.tokens, w.head_dim
     layer = synth.make_workload(w, device=dev)
     qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
     kv_ref = oracle.kv(kb, vb)
-    rows = sampled_rows(H, N, 4096, 1)
-    ref = oracle.apply_rows(qb, kv_ref, den, rows)
+    ref = torch.from_numpy(oracle.apply_rows(qb, kv_ref, den).reshape(H, N, D)).to(dev)
+    tm = {k: to_token_major(layer[k]) for k in ("q_rot", "k_rot", "v")}
     with la.LinAttn(H, N, D, dev) as ctx:
         for mode in MODES:
             for dt in (torch.float32, torch.bfloat16):
                 out = run(ctx, layer, mode, dt)
-                got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
-                err = rel_l2(got, ref)
-                assert err <= TOL[dt], f"{name} {mode} {dt}: sampled rel-L2 {err:.3e}"
+                check_whole(out, ref, dt, f"{name} {mode} {dt}")
                 kv_err = rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref)
                 assert kv_err <= KV_TOL, f"{name} {mode}: KV rel-L2 {kv_err:.3e}"
+                nhd = ctx.forward(tm["q_rot"], tm["k_rot"], tm["v"], layer["den"], mode=mode, out_dtype=dt,
+                                  layout="nhd")
+                assert ctx.device_status() == 0
+                assert torch.equal(nhd.view(1, N, H, D), to_token_major(out)), (name, mode, dt)
+                del out, nhd
 
 
 @pytest.mark.parametrize("n", synth.SWEEP_TOKENS)
-def test_token_sweep_sampled(la, dev, n):
-    """The N sweep at H=20, D=112 and at H=32, D=64: KV whole, output on sampled rows."""
+def test_token_sweep_whole_tensor(la, dev, n):
+    """The N sweep at H=20, D=112 and at H=32, D=64: every output element and the KV against
+    the oracle (FP32 output in both tiers; BF16 output too at N = 65536)."""
     for name in (f"sweep_n{n}", f"sweep_n{n}_d64"):
         w = synth.WORKLOADS[name]
         H, N, D = w.heads, w.tokens, w.head_dim
         layer = synth.make_workload(w, device=dev)
         qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
         kv_ref = oracle.kv(kb, vb)
-        rows = sampled_rows(H, N, 2048, n)
-        ref = oracle.apply_rows(qb, kv_ref, den, rows)
+        ref = torch.from_numpy(oracle.apply_rows(qb, kv_ref, den).reshape(H, N, D)).to(dev)
+        dtypes = (torch.float32, torch.bfloat16) if n == 65536 else (torch.float32,)
         with la.LinAttn(H, N, D, dev) as ctx:
             for mode in MODES:
-                out = run(ctx, layer, mode, torch.float32)
-                got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
-                assert rel_l2(got, ref) <= TOL[torch.float32], (name, mode)
+                for dt in dtypes:
+                    check_whole(run(ctx, layer, mode, dt), ref, dt, f"{name} {mode} {dt}")
                 assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= KV_TOL, (name, mode)
 
 
 def test_denoise_step_twenty_layers(la, dev):
     """20 sequential layer calls at the 720p shape with fresh seeded inputs per layer on one
     context (the scratch is reused call after call); the first and last layers are held to
-    the oracle on sampled rows, every call must finish with a clean status."""
+    the oracle on every output element, every call must finish with a clean status."""
     w = synth.WORKLOADS["720p_193f"]
     H, N, D = w.heads, w.tokens, w.head_dim
     out = torch.empty(1, H, N, D, device=dev)
@@ -160,11 +168,8 @@ def test_denoise_step_twenty_layers(la, dev):
                 if layer_idx in (0, synth.DENOISE_LAYERS - 1):
                     assert ctx.device_status() == 0
                     qb, kb, vb, den = oracle.torch_inputs_to_numpy(layer)
-                    kv_ref = oracle.kv(kb, vb)
-                    rows = sampled_rows(H, N, 1024, layer_idx)
-                    ref = oracle.apply_rows(qb, kv_ref, den, rows)
-                    got = out.reshape(H * N, D)[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
-                    assert rel_l2(got, ref) <= TOL[torch.float32], (mode, layer_idx)
+                    ref = oracle.apply_rows(qb, oracle.kv(kb, vb), den).reshape(H, N, D)
+                    check_whole(out, ref, torch.float32, f"denoise {mode} layer {layer_idx}")
             assert ctx.device_status() == 0
 
 
@@ -285,11 +290,6 @@ def test_ragged_tail_stores_repeated(la, dev, N):
             assert err <= TOL[dt], f"N={N} {dt}: rel-L2 {err:.3e}"
             for _ in range(8):
                 assert torch.equal(run(ctx, g, "high", dt), first)
-
-
-def to_token_major(t):
-    """[1, H, N, D] -> contiguous [1, N, H, D]."""
-    return t.permute(0, 2, 1, 3).contiguous()
 
 
 @pytest.mark.parametrize("shape", [(20, 3001, 112), (3, 777, 64), (2, 256, 32), (5, 129, 128)])

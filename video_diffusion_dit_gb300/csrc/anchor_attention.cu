@@ -83,7 +83,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     anchor_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, int n_tokens,
-                            int head_dim, float scale_log2, int* status) {
+                            int head_dim, float scale_log2, int* status, uint64_t wait_ns) {
     using L = AttnLayout<NBOX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -151,13 +151,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      pol_q);
             const uint32_t n_loads = 2u * static_cast<uint32_t>(n_kv);
             uint32_t i = 0;
-            bool ok = true;
             for (; i < n_loads; ++i) {
                 const uint32_t st = i % kSlots, ph = (i / kSlots) & 1u;
-                if (!mbar_wait(kv_empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(kv_empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
                 mbar_arrive_expect_tx(kv_full0 + 8u * st, L::tile_bytes);
                 const CUtensorMap* map = (i & 1u) ? &tm_v : &tm_k;
                 const int key0 = static_cast<int>(i >> 1) * kBN;
@@ -165,11 +161,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int x = 0; x < NBOX; ++x)
                     tma_load_3d(slot_addr(i) + x * kAtom, map, kv_full0 + 8u * st, 64 * x, key0, h);
             }
-            if (!ok) {  // let the copies in flight land before the CTA exits
-                const uint32_t first = i > kSlots ? i - kSlots : 0;
-                for (uint32_t k = first; k < i; ++k) mbar_wait_drain(kv_full0 + 8u * (k % kSlots), (k / kSlots) & 1u);
-                mbar_wait_drain(q_full, 0);
-            }
+            // Let the copies in flight land before the CTA exits: the MMA issuer waits for all
+            // of them unless some role gave up, in which case nothing else would.
+            const uint32_t first = i > kSlots ? i - kSlots : 0;
+            for (uint32_t k = first; k < i; ++k) mbar_wait_drain(kv_full0 + 8u * (k % kSlots), (k / kSlots) & 1u);
+            mbar_wait_drain(q_full, 0);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
@@ -178,7 +174,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t idesc_o = make_idesc_bf16_f32(kBM, head_dim, false, true);  // P K-major (TMEM), V MN-major
             const int ksteps = head_dim / 16;
             auto wait_full = [&](uint32_t i) {
-                return mbar_wait(kv_full0 + 8u * (i % kSlots), (i / kSlots) & 1u, abort_flag, status);
+                return mbar_wait(kv_full0 + 8u * (i % kSlots), (i / kSlots) & 1u, abort_flag, status, wait_ns);
             };
             auto issue_s = [&](int t, uint32_t kslot) {
                 const uint32_t qa = base + t * L::tile_bytes;
@@ -196,7 +192,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 make_smem_desc(vslot + kk * 2048u, kAtom, 1024u, kSwizzle128B), idesc_o,
                                 (accumulate || kk != 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(q_full, 0, abort_flag, status) && wait_full(0);
+            bool ok = mbar_wait(q_full, 0, abort_flag, status, wait_ns) && wait_full(0);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, slot_addr(0));
@@ -206,7 +202,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (uint32_t j = 0; ok && j < static_cast<uint32_t>(n_kv); ++j) {
                 const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
                 const bool more = j + 1 < static_cast<uint32_t>(n_kv);
-                if (!(ok = wait_full(iv) && mbar_wait(p_full0, j & 1u, abort_flag, status))) break;
+                if (!(ok = wait_full(iv) && mbar_wait(p_full0, j & 1u, abort_flag, status, wait_ns))) break;
                 tc_fence_after();
                 issue_pv(0, slot_addr(iv), j > 0);
                 if (more) {
@@ -214,7 +210,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after();
                     issue_s(0, slot_addr(ik));
                 }
-                if (!(ok = mbar_wait(p_full0 + 8u, j & 1u, abort_flag, status))) break;
+                if (!(ok = mbar_wait(p_full0 + 8u, j & 1u, abort_flag, status, wait_ns))) break;
                 tc_fence_after();
                 issue_pv(1, slot_addr(iv), j > 0);
                 mma_commit(kv_empty0 + 8u * (iv % kSlots));
@@ -238,7 +234,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            if (!(ok = mbar_wait(s_full0 + 8u * t, j & 1u, abort_flag, status))) break;
+            if (!(ok = mbar_wait_warp(s_full0 + 8u * t, j & 1u, abort_flag, status, wait_ns))) break;
             tc_fence_after();
             // The whole row of S_t(j); keys past the end are masked out.
             const int valid = min(kBN, n_tokens - j * kBN);
@@ -286,7 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive(p_full0 + 8u * t);
         }
         // Epilogue: O_t / l once the last product has landed.
-        if (ok && mbar_wait(o_done, 0, abort_flag, status)) {
+        if (ok && mbar_wait_warp(o_done, 0, abort_flag, status, wait_ns)) {
             tc_fence_after();
             const int row = m0 + kBM * t + r;
             const float inv = 1.0f / l;
@@ -329,14 +325,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 template <int NBOX, bool BF16>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* out, int heads,
-                   int n_tokens, int head_dim, float scale_log2, int* status, cudaStream_t stream) {
+                   int n_tokens, int head_dim, float scale_log2, int* status, uint64_t wait_ns,
+                   cudaStream_t stream) {
     using L = AttnLayout<NBOX>;
     cudaError_t e = cudaFuncSetAttribute(anchor_attention_kernel<NBOX, BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
     if (e != cudaSuccess) return e;
     const int q_blocks = (n_tokens + kQTiles * kBM - 1) / (kQTiles * kBM);
     anchor_attention_kernel<NBOX, BF16><<<heads * q_blocks, kAttnThreads, L::smem_bytes, stream>>>(
-        tq, tk, tv, out, n_tokens, head_dim, scale_log2, status);
+        tq, tk, tv, out, n_tokens, head_dim, scale_log2, status, wait_ns);
     return cudaGetLastError();
 }
 
@@ -344,13 +341,13 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 cudaError_t launch_anchor_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     void* out, bool out_bf16, int heads, int64_t n_tokens, int head_dim,
-                                    float scale_log2, int* status, cudaStream_t stream) {
+                                    float scale_log2, int* status, uint64_t wait_ns, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
     if (head_dim_atoms(head_dim) == 1)
-        return out_bf16 ? launch<1, true>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, stream)
-                        : launch<1, false>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, stream);
-    return out_bf16 ? launch<2, true>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, stream)
-                    : launch<2, false>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, stream);
+        return out_bf16 ? launch<1, true>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, wait_ns, stream)
+                        : launch<1, false>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, wait_ns, stream);
+    return out_bf16 ? launch<2, true>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, wait_ns, stream)
+                    : launch<2, false>(tm_q, tm_k, tm_v, out, heads, n, head_dim, scale_log2, status, wait_ns, stream);
 }
 
 }  // namespace la

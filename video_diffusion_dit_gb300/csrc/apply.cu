@@ -48,7 +48,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kApplyThreads, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                     const uint8_t* __restrict__ kv_image, const float* __restrict__ den, int heads, int n_tokens,
-                    int head_dim, int tiles_per_head, int token_major, int* status) {
+                    int head_dim, int tiles_per_head, int token_major, int* status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -130,15 +130,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             uint32_t it = 0;
             int cur_h = -1, run = -1;
-            bool ok = true, b_pending = false;
+            bool b_pending = false;
             for (int t = t_begin; t < t_end; ++t, ++it) {
                 const int h = t / tiles_per_head;
                 const int n0 = (t % tiles_per_head) * kApplyTile;
                 const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
-                if (!mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kQAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
@@ -151,9 +148,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                     }
                     ++run;
                     cur_h = h;
-                    if (run > 0 && !mbar_wait(b_empty, (run - 1) & 1, abort_flag, status)) {
-                        ++it;
-                        ok = false;
+                    if (run > 0 && !mbar_wait(b_empty, (run - 1) & 1, abort_flag, status, wait_ns)) {
+                        ++it;  // this tile's Q load was issued
+                        --run;  // ... but not this head's image
                         break;
                     }
                     mbar_arrive_expect_tx(b_full, img_bytes);
@@ -161,12 +158,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                     b_pending = true;
                 }
             }
-            if (!ok) {
-                const uint32_t first = it > kApplyStages ? it - kApplyStages : 0;
-                for (uint32_t j = first; j < it; ++j)
-                    mbar_wait_drain(q_full0 + 8u * (j % kApplyStages), (j / kApplyStages) & 1u);
-                if (b_pending) mbar_wait_drain(b_full, run & 1);
-            }
+            // Let the copies already issued land before shared memory goes away: the MMA
+            // issuer waits for all of them unless some role gave up, in which case nothing
+            // else would.  (`it` Q loads were issued, only the last kApplyStages can be
+            // pending; image `run` is the only image load that can be.)
+            const uint32_t first = it > kApplyStages ? it - kApplyStages : 0;
+            for (uint32_t j = first; j < it; ++j)
+                mbar_wait_drain(q_full0 + 8u * (j % kApplyStages), (j / kApplyStages) & 1u);
+            if (b_pending) mbar_wait_drain(b_full, run & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -181,14 +180,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                     if (run >= 0) mma_commit(b_empty);  // old image free once its MMAs are done
                     ++run;
                     cur_h = h;
-                    if (!mbar_wait(b_full, run & 1, abort_flag, status)) break;
+                    if (!mbar_wait(b_full, run & 1, abort_flag, status, wait_ns)) break;
                     tc_fence_after();
                 }
                 const uint32_t buf = lt & 1u;
-                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
-                if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
+                if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 128u;
                 const uint32_t qa = q_smem + st * NBOX * kQAtomBytes;
@@ -229,7 +228,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             const uint32_t buf = lt & 1u;
             const float dv = row < n_tokens ? den[static_cast<int64_t>(h) * n_tokens + row] : 1.0f;
             const float rcp = __frcp_rn(dv);
-            if (!mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status)) break;
+            if (!mbar_wait_warp(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
             // A warp whose 32 rows all lie past the end of the head (ragged last tile) has
@@ -294,21 +293,21 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
 template <int NBOX, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
                       int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
-                      cudaStream_t stream) {
+                      uint64_t wait_ns, cudaStream_t stream) {
     const uint32_t smem = apply_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
     return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
-                             img, den, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status);
+                             img, den, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, wait_ns);
 }
 
 }  // namespace
 
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, cudaStream_t stream) {
+                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream) {
     const int n = static_cast<int>(n_tokens);
     const int tph = (n + kApplyTile - 1) / kApplyTile;
     const int total = heads * tph;
@@ -319,10 +318,10 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
     }
     const bool one = head_dim_atoms(head_dim) == 1;
     if (one)
-        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
-                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
-    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream)
-                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, stream);
+        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream)
+                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream);
+    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream)
+                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream);
 }
 
 }  // namespace la

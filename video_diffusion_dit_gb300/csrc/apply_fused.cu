@@ -42,10 +42,7 @@ constexpr int kFXfWarp0 = 2 + kFEpiWarps;
 constexpr int kFThreads = 32 * (kFXfWarp0 + kFXfWarps);
 constexpr int kFTransformThreads = 32 * kFXfWarps;
 constexpr int kFRowGroups = kFTransformThreads / 16;  // a transform thread takes rows rg + kFRowGroups k
-#ifndef LA_FUSED_TAB_SUBS
-#define LA_FUSED_TAB_SUBS 2
-#endif
-constexpr int kFTabSubs = LA_FUSED_TAB_SUBS;        // table slots per tile
+constexpr int kFTabSubs = 2;                        // table slots per tile (half a tile of rows each)
 constexpr int kFTabSlots = 3 * kFTabSubs / 2;       // table ring: 1.5 tiles of rows
 constexpr uint32_t kFOutBufs = 1;                   // staging buffers per epilogue warp
 // Reciprocal-denominator buffers between the transform and the epilogue.  A buffer is
@@ -82,7 +79,8 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
     apply_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                        const uint8_t* __restrict__ kv_image, int heads, int n_tokens, int head_dim,
-                       int tiles_per_head, int token_major, int* status, const ProducerArgs pa) {
+                       int tiles_per_head, int token_major, int* status, uint64_t wait_ns,
+                       const ProducerArgs pa) {
     constexpr int kStages = fused_stages(NBOX);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -181,7 +179,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int h = t / tiles_per_head;
                 const int n0 = (t % tiles_per_head) * kApplyTile;
                 const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
-                if (!(ok = mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status))) break;
+                if (!(ok = mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns))) break;
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kFQAtom);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
@@ -193,7 +191,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 for (uint32_t hh = 0; hh < kFTabSubs && ok; ++hh) {
                     const uint32_t i = kFTabSubs * it + hh;
                     const uint32_t slot = i % kFTabSlots, tph = (i / kFTabSlots) & 1u;
-                    if (!(ok = mbar_wait(tab_empty0 + 8u * slot, tph ^ 1u, abort_flag, status))) break;
+                    if (!(ok = mbar_wait(tab_empty0 + 8u * slot, tph ^ 1u, abort_flag, status, wait_ns))) break;
                     const int r0 = n0 + static_cast<int>(hh) * kFTabRows;
                     const int rows = max(0, min(kFTabRows, n_tokens - r0));
                     const uint32_t bytes = static_cast<uint32_t>(rows) * row_bytes;
@@ -208,14 +206,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     tab_issued = i + 1;
                 }
             }
-            if (!ok) {  // let the copies in flight land before the CTA exits
-                const uint32_t first = q_issued > kStages ? q_issued - kStages : 0;
-                for (uint32_t j = first; j < q_issued; ++j)
-                    mbar_wait_drain(q_full0 + 8u * (j % kStages), (j / kStages) & 1u);
-                const uint32_t tfirst = tab_issued > kFTabSlots ? tab_issued - kFTabSlots : 0u;
-                for (uint32_t j = tfirst; j < tab_issued; ++j)
-                    mbar_wait_drain(tab_full0 + 8u * (j % kFTabSlots), (j / kFTabSlots) & 1u);
-            }
+            // Let the copies in flight land before the CTA exits: the consumers wait for all of
+            // them unless some role gave up, in which case nothing else would.
+            const uint32_t first = q_issued > kStages ? q_issued - kStages : 0;
+            for (uint32_t j = first; j < q_issued; ++j)
+                mbar_wait_drain(q_full0 + 8u * (j % kStages), (j / kStages) & 1u);
+            const uint32_t tfirst = tab_issued > kFTabSlots ? tab_issued - kFTabSlots : 0u;
+            for (uint32_t j = tfirst; j < tab_issued; ++j)
+                mbar_wait_drain(tab_full0 + 8u * (j % kFTabSlots), (j / kFTabSlots) & 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -231,13 +229,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     if (run >= 0) mma_commit(b_empty);  // the old image is free once its MMAs are done
                     ++run;
                     cur_h = h;
-                    if (!mbar_wait(b_full, run & 1, abort_flag, status)) break;
+                    if (!mbar_wait(b_full, run & 1, abort_flag, status, wait_ns)) break;
                     tc_fence_after();
                 }
                 const uint32_t buf = lt & 1u;
-                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status, wait_ns)) break;
                 const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
-                if (!mbar_wait(q_ready0 + 8u * st, ph, abort_flag, status)) break;
+                if (!mbar_wait(q_ready0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * kFAccCols;
                 const uint32_t qb = q_smem + st * NBOX * kFQAtom;
@@ -287,15 +285,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
             const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
-            if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status)) break;
-            if (!mbar_wait(den_empty0 + 8u * db, dph ^ 1u, abort_flag, status)) break;
+            if (!mbar_wait_warp(q_full0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
+            if (!mbar_wait_warp(den_empty0 + 8u * db, dph ^ 1u, abort_flag, status, wait_ns)) break;
             uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kFQAtom;
             bool ok = true;
 #pragma unroll
             for (int hh = 0; hh < kFTabSubs; ++hh) {
                 const uint32_t i = kFTabSubs * it + hh;
                 const uint32_t slot = i % kFTabSlots;
-                if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status))) break;
+                if (!(ok = mbar_wait_warp(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status, wait_ns))) break;
                 const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;
                 constexpr int kPer = kFTabRows / kFRowGroups;  // this thread's rows per slot
 #pragma unroll
@@ -359,7 +357,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (cur_h < 0) grid_dependency_wait();
                 ++run;
                 cur_h = h;
-                if (run > 0 && !(ok = mbar_wait(b_empty, (run - 1) & 1, abort_flag, status))) break;
+                if (run > 0 && !(ok = mbar_wait_warp(b_empty, (run - 1) & 1, abort_flag, status, wait_ns))) break;
                 tc_fence_after();
                 const uint8_t* img = kv_image + static_cast<int64_t>(h) * 3 * term_bytes;
                 const uint32_t groups = 3u * half_d / 8u;  // 8-word groups of the three terms
@@ -391,8 +389,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             const uint32_t buf = lt & 1u;
             const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
-            if (!(ok = mbar_wait(den_full0 + 8u * db, dph, abort_flag, status))) break;
-            if (!(ok = mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status))) break;
+            if (!(ok = mbar_wait_warp(den_full0 + 8u * db, dph, abort_flag, status, wait_ns))) break;
+            if (!(ok = mbar_wait_warp(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns))) break;
             tc_fence_after();
             const float* rcp_t = rcp_s + db * kApplyTile;
             for (int g = 2 * e; g < 2 * e + 2 && n0 + 32 * g < n_tokens; ++g) {
@@ -449,21 +447,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
 template <int NBOX, bool BF16>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, int heads, int n_tokens,
-                   int head_dim, bool token_major, int grid, int* status, cudaStream_t stream, const ProducerArgs& pa) {
+                   int head_dim, bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream,
+                   const ProducerArgs& pa) {
     const uint32_t smem = fused_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_fused_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
     return launch_overlapped(apply_fused_kernel<NBOX, BF16>, dim3(grid), dim3(kFThreads), smem, stream, tm_q, tm_out,
-                             img, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, pa);
+                             img, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, wait_ns, pa);
 }
 
 }  // namespace
 
 cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out_t, const uint8_t* kv_image,
                                   int heads, int64_t n_tokens, int head_dim, bool out_bf16, bool token_major, int grid,
-                                  int* status, cudaStream_t stream, const ProducerArgs& producer) {
+                                  int* status, uint64_t wait_ns, cudaStream_t stream, const ProducerArgs& producer) {
     const int n = static_cast<int>(n_tokens);
     const int tph = (n + kApplyTile - 1) / kApplyTile;
     const int total = heads * tph;
@@ -473,10 +472,10 @@ cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm
         grid = k * heads;
     }
     if (head_dim_atoms(head_dim) == 1)
-        return out_bf16 ? launch<1, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer)
-                        : launch<1, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer);
-    return out_bf16 ? launch<2, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer)
-                    : launch<2, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, stream, producer);
+        return out_bf16 ? launch<1, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer)
+                        : launch<1, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer);
+    return out_bf16 ? launch<2, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer)
+                    : launch<2, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer);
 }
 
 }  // namespace la

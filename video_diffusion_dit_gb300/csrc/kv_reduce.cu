@@ -72,7 +72,7 @@ template <int NBOX, bool FUSED, int PROMOTE>
 __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     kv_partial_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          float* __restrict__ partial, int head_dim, const KvPlan plan, const KvLaunch work,
-                         int token_major, int* status, const ProducerArgs pa,
+                         int token_major, int* status, uint64_t wait_ns, const ProducerArgs pa,
                          const __grid_constant__ CUtensorMap tm_cos, const __grid_constant__ CUtensorMap tm_sin) {
     using L = KvLayout<NBOX, FUSED>;
     extern __shared__ uint8_t smem_raw[];
@@ -149,16 +149,12 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             const uint64_t tab_pol = policy_evict_last();
             uint32_t it = 0;
-            bool ok = true;
             for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
                 const int h = static_cast<int>(t / tph);
                 const int y = static_cast<int>((t % tph) * kKvTile);
                 const int c1 = token_major ? h - work.h0 : y, c2 = token_major ? y : h - work.h0;
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
-                if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
                 const uint32_t a = base + st * L::stage_bytes;
                 const uint32_t b = a + L::a_bytes;
                 const uint32_t tab_tx = FUSED ? 2u * kKvTile * (head_dim / 2) * 4u : 0u;
@@ -175,12 +171,12 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     tma_load_2d_hint(tab + L::tab_bytes, &tm_sin, full0 + 8u * st, 0, y, tab_pol);
                 }
             }
-            if (!ok) {
-                // Let the loads already issued land before shared memory goes away.
-                const uint32_t first = it > L::stages ? it - L::stages : 0;
-                for (uint32_t j = first; j < it; ++j)
-                    mbar_wait_drain(full0 + 8u * (j % L::stages), (j / L::stages) & 1u);
-            }
+            // Let the loads already issued land before shared memory goes away: the MMA
+            // issuer waits for all of them unless some role gave up, in which case nothing
+            // else would.  (`it` loads were issued; only the last `stages` can be pending.)
+            const uint32_t first = it > L::stages ? it - L::stages : 0;
+            for (uint32_t j = first; j < it; ++j)
+                mbar_wait_drain(full0 + 8u * (j % L::stages), (j / L::stages) & 1u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -197,7 +193,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                 for (int64_t k0 = t; ok && k0 < seg_end; k0 += PROMOTE, ++sub) {
                     const int64_t k1 = min(k0 + PROMOTE, seg_end);
                     const uint32_t buf = sub & 1u;
-                    if (!mbar_wait(acc_empty0 + 8u * buf, ((sub >> 1) & 1u) ^ 1u, abort_flag, status)) {
+                    if (!mbar_wait(acc_empty0 + 8u * buf, ((sub >> 1) & 1u) ^ 1u, abort_flag, status, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -205,7 +201,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     const uint32_t d = tmem + buf * 128u;
                     for (int64_t k = k0; k < k1; ++k, ++it) {
                         const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
-                        if (!mbar_wait(mma_ready0 + 8u * st, ph, abort_flag, status)) {
+                        if (!mbar_wait(mma_ready0 + 8u * st, ph, abort_flag, status, wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -248,7 +244,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             for (int e = 0; e < 4; ++e) ks[e] = kc[e] = 0ull;
             for (; t < seg_end; ++t, ++it) {
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
-                if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status)) {
+                if (!mbar_wait_warp(full0 + 8u * st, ph, abort_flag, status, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -323,7 +319,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             }
             for (int64_t k0 = t; k0 < seg_end; k0 += PROMOTE, ++sub) {
                 const uint32_t buf = sub & 1u;
-                if (!mbar_wait(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status)) {
+                if (!mbar_wait_warp(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -539,23 +535,24 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restric
 
 template <int NBOX, bool FUSED, int PROMOTE>
 cudaError_t launch_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int head_dim,
-                      const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, cudaStream_t stream,
-                      const ProducerArgs& pa, const CUtensorMap& tm_cos, const CUtensorMap& tm_sin) {
+                      const KvPlan& plan, const KvLaunch& work, bool token_major, int* status, uint64_t wait_ns,
+                      cudaStream_t stream, const ProducerArgs& pa, const CUtensorMap& tm_cos,
+                      const CUtensorMap& tm_sin) {
     using L = KvLayout<NBOX, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(kv_partial_tc_kernel<NBOX, FUSED, PROMOTE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::smem_bytes);
     if (e != cudaSuccess) return e;
     return launch_overlapped(kv_partial_tc_kernel<NBOX, FUSED, PROMOTE>, dim3(work.n_chunks),
                              dim3(FUSED ? kKvThreadsFused : kKvThreads), L::smem_bytes, stream, tm_k, tm_v, partial,
-                             head_dim, plan, work, token_major ? 1 : 0, status, pa, tm_cos, tm_sin);
+                             head_dim, plan, work, token_major ? 1 : 0, status, wait_ns, pa, tm_cos, tm_sin);
 }
 
 }  // namespace
 
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
                                  int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major,
-                                 bool lossless, int* status, cudaStream_t stream, const ProducerArgs* producer,
-                                 const CUtensorMap* tm_tables) {
+                                 bool lossless, int* status, uint64_t wait_ns, cudaStream_t stream,
+                                 const ProducerArgs* producer, const CUtensorMap* tm_tables) {
     (void)n_tokens;
     const ProducerArgs pa = producer ? *producer : ProducerArgs{nullptr, nullptr, nullptr, nullptr, 0};
     const CUtensorMap none{};
@@ -563,7 +560,7 @@ cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_
     const CUtensorMap& ts = tm_tables ? tm_tables[1] : none;
     const bool one = head_dim_atoms(head_dim) == 1;
 #define LA_KV_LAUNCH(NB, FU, PR) \
-    launch_tc<NB, FU, PR>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, stream, pa, tc, ts)
+    launch_tc<NB, FU, PR>(tm_k, tm_v, partial, head_dim, plan, work, token_major, status, wait_ns, stream, pa, tc, ts)
     if (producer && lossless)
         return one ? LA_KV_LAUNCH(1, true, kPromoteLossless) : LA_KV_LAUNCH(2, true, kPromoteLossless);
     if (producer) return one ? LA_KV_LAUNCH(1, true, kPromoteHigh) : LA_KV_LAUNCH(2, true, kPromoteHigh);

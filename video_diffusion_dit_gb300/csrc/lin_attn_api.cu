@@ -23,6 +23,7 @@ struct lin_attn_ctx {
     float* kv = nullptr;          // [heads][D][D] FP32 reduced KV
     uint8_t* kv_image = nullptr;  // [heads] x three-term BF16 image for the tensor-core apply
     int* status = nullptr;        // device status word (LIN_ATTN_ERR_TIMEOUT if a kernel gave up)
+    uint64_t wait_ns = la::kWaitLimitNs;  // how long a kernel waits on one of its barriers before giving up
     double* ksum_partial = nullptr;  // fused path: [heads][seg_stride_alloc][row groups][D] FP64 column sums of relu(K)
     float* ksum = nullptr;           // fused path: [heads][D] FP32 reduced column sums
     // host-buffer path staging, allocated on first use
@@ -218,8 +219,8 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                 if (rc) return rc;
             }
         }
-        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, lossless, c->status, stream,
-                                     fused ? &pa_kv : nullptr, fused ? tabs : nullptr);
+        e = la::launch_kv_partial_tc(tk, tv, c->partial, n_tokens, D, plan, work, tm, lossless, c->status, c->wait_ns,
+                                     stream, fused ? &pa_kv : nullptr, fused ? tabs : nullptr);
         if (e != cudaSuccess) return cuda_fail(e, "kv_partial_tc launch");
     }
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -236,13 +237,14 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H,
                                      CU_TENSOR_MAP_SWIZZLE_NONE);
             if (rc) return rc;
-            e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status,
+            e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, c->wait_ns,
                                           stream, pa_apply);
         } else {
             rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
             if (rc) return rc;
-            e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, stream);
+            e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, c->wait_ns,
+                                    stream);
         }
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     }
@@ -448,7 +450,8 @@ int lin_attn_anchor_forward(lin_attn_ctx* ctx, const void* q, const void* k, con
     if ((rc = make_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128))) return rc;
     if ((rc = make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, H, 64, 128))) return rc;
     cudaError_t e = la::launch_anchor_attention(tq, tk, tv, out, out_dtype == LIN_ATTN_OUT_BF16, H, n_tokens, D,
-                                                s * log2e, ctx->status, reinterpret_cast<cudaStream_t>(stream));
+                                                s * log2e, ctx->status, ctx->wait_ns,
+                                                reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "anchor_attention launch");
     return ok();
 }
@@ -560,6 +563,15 @@ int lin_attn_device_status(lin_attn_ctx* ctx, struct CUstream_st* stream) {
         cudaMemset(ctx->status, 0, sizeof(int));
         return fail(h, "a kernel reported status %d (%s)", h, lin_attn_error_string(h));
     }
+    return ok();
+}
+
+int lin_attn_set_wait_limit(lin_attn_ctx* ctx, uint64_t limit_ns) {
+    if (!ctx) return fail(LIN_ATTN_ERR_INVALID_ARG, "ctx is NULL");
+    if (limit_ns > la::kWaitLimitNs)
+        return fail(LIN_ATTN_ERR_INVALID_ARG, "limit_ns=%llu exceeds the default %llu", (unsigned long long)limit_ns,
+                    (unsigned long long)la::kWaitLimitNs);
+    ctx->wait_ns = limit_ns == 0 ? la::kWaitLimitNs : limit_ns;
     return ok();
 }
 

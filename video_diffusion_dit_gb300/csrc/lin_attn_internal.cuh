@@ -136,10 +136,7 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 //                  sums of relu(K) (scratch)
 //   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
 // Row groups of the fused KV kernel's transform (one column-sum partial each).
-#ifndef LA_KSUM_GROUPS
-#define LA_KSUM_GROUPS 16
-#endif
-constexpr int kKsumGroups = LA_KSUM_GROUPS;
+constexpr int kKsumGroups = 16;
 struct ProducerArgs {
     const float* cos;
     const float* sin;
@@ -193,8 +190,8 @@ __device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const floa
 // (D/2, N), box (D/2, 64), no swizzle).
 cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, float* partial, int64_t n_tokens,
                                  int head_dim, const KvPlan& plan, const KvLaunch& work, bool token_major,
-                                 bool lossless, int* status, cudaStream_t stream, const ProducerArgs* producer = nullptr,
-                                 const CUtensorMap* tm_tables = nullptr);
+                                 bool lossless, int* status, uint64_t wait_ns, cudaStream_t stream,
+                                 const ProducerArgs* producer = nullptr, const CUtensorMap* tm_tables = nullptr);
 
 // Fixed-order pairwise reduction of each head's partials for heads [h0, h0 + hc):
 // kv[h][i][j] (FP32) and, if kv_image != nullptr, its three-term BF16 image for the
@@ -205,7 +202,7 @@ cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_imag
 // out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms (maps as above).
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, cudaStream_t stream);
+                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream);
 
 // Softmax anchor attention (flash forward): out = softmax(scale * Q K^T) V per head, no
 // mask.  Maps over [H][N][D] BF16: Q box (64, 128), K and V boxes (64, 64); scale_log2 =
@@ -215,10 +212,10 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
 // 32 tokens) box and no swizzle; both index (column, head, token) if token_major.
 cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out_t, const uint8_t* kv_image,
                                   int heads, int64_t n_tokens, int head_dim, bool out_bf16, bool token_major, int grid,
-                                  int* status, cudaStream_t stream, const ProducerArgs& producer);
+                                  int* status, uint64_t wait_ns, cudaStream_t stream, const ProducerArgs& producer);
 
 cudaError_t launch_anchor_attention(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                     void* out, bool out_bf16, int heads, int64_t n_tokens, int head_dim,
-                                    float scale_log2, int* status, cudaStream_t stream);
+                                    float scale_log2, int* status, uint64_t wait_ns, cudaStream_t stream);
 
 }  // namespace la

@@ -12,8 +12,9 @@
 // The array (kNoAllocScratchBytes) is a file-scope __device__ variable, so every GPU that
 // loads this library holds it until the process exits.  Its host-side name is only a
 // stand-in for the symbol, never a device address: the first call on each device (with
-// that device current) resolves the real address once with cudaGetSymbolAddress and
-// caches it, and that first call should therefore come before any stream capture.  All
+// that device current) resolves the real address with cudaGetSymbolAddress and caches it
+// (a failed attempt is not cached; the next call retries), and that first call should
+// therefore come before any stream capture.  All
 // calls share the array and it keeps the previous call's contents: the parts that must
 // start at zero are cleared by every call, and calls whose execution overlaps on the GPU
 // (two streams, or two host threads) race on it and give wrong results.
@@ -33,14 +34,17 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Per-device set-up.  Only a successful set-up is kept: if resolving the address fails
+// (for instance because the first call was made while a stream was being captured), the
+// next call on that device tries again.
 struct DeviceSetup {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    bool resolved = false;
     unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int n_sms = 0;
     bool supported = false;
 };
 DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_mutex;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -121,17 +125,30 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (device < 0 || device >= kMaxDevices) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device index %d too large", device);
-    DeviceSetup& su = g_setup[device];
-    std::call_once(su.once, [&su, device] {
-        int major = 0, minor = 0;
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
-        cudaDeviceGetAttribute(&su.n_sms, cudaDevAttrMultiProcessorCount, device);
-        su.supported = major == 10 && minor == 3;
-        if (su.supported) su.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&su.scratch), g_noalloc_scratch);
-    });
-    if (!su.supported) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is not sm_103", device);
-    if (su.err != cudaSuccess || !su.scratch) return cuda_fail(su.err, "cudaGetSymbolAddress(scratch)");
+    DeviceSetup su;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        DeviceSetup& slot = g_setup[device];
+        if (!slot.resolved) {
+            int major = 0, minor = 0, sms = 0;
+            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+                return cuda_fail(e, "cudaDeviceGetAttribute");
+            if (major != 10 || minor != 3) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is not sm_103", device);
+            unsigned char* addr = nullptr;
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&addr), g_noalloc_scratch);
+            if (e != cudaSuccess || !addr) {
+                cudaGetLastError();  // not sticky; leave the set-up open for the next call
+                return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+            }
+            slot.scratch = addr;
+            slot.n_sms = sms;
+            slot.supported = true;
+            slot.resolved = true;
+        }
+        su = slot;
+    }
 
     float* partial = reinterpret_cast<float*>(su.scratch);
     float* kv = reinterpret_cast<float*>(su.scratch + partial_bytes);
@@ -150,7 +167,7 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
         !make_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, la::kKvTile))
         return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = la::launch_kv_partial_tc(tk, tv, partial, n_tokens, head_dim, plan, work, false, mode == LIN_ATTN_MODE_LOSSLESS,
-                                 status, s);
+                                 status, la::kWaitLimitNs, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_partial launch");
     e = la::launch_kv_finalize(partial, kv, image, 0, heads, head_dim, plan, s);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
@@ -160,7 +177,8 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
     const bool oko = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, head_dim, n_tokens, heads, 64, 32)
                               : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, head_dim, n_tokens, heads, 32, 32);
     if (!okq || !oko) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status, s);
+    e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status,
+                            la::kWaitLimitNs, s);
     if (e != cudaSuccess) return cuda_fail(e, "apply launch");
     return la::record_error(LIN_ATTN_OK, "");
 }

@@ -7,8 +7,10 @@
 
 namespace la {
 
-// Every wait on a barrier gives up after this long, flags the CTA and the context status
-// word, and lets the kernel wind down instead of spinning forever.
+// Every wait on a barrier gives up after a limit (by default this long; a context may set
+// a shorter one for tests), flags the CTA and the context status word, and lets the kernel
+// wind down instead of spinning forever.  The waits that let copies and MMAs already in
+// flight land while winding down always use this default.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kStatusTimeout = 6;                  // LIN_ATTN_ERR_TIMEOUT
 
@@ -48,21 +50,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Limits below this are probed with the non-blocking test_wait, so that the limit itself -
+// not the hardware's own suspend window inside try_wait - decides when a wait gives up.
+constexpr uint64_t kBlockingProbeMinNs = 1000000ull;  // 1 ms
+
 // Wait for the phase with the given parity to complete.  Returns false (without the
-// phase completing) if the CTA's abort flag is raised or the time limit passes; in the
-// latter case it raises the abort flag and records a timeout in the status word.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// phase completing) if the CTA's abort flag is raised or `limit_ns` passes; in the latter
+// case it raises the abort flag and records a timeout in the status word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit_ns) {
+    const bool poll = limit_ns < kBlockingProbeMinNs;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicExch(status, kStatusTimeout);
             return false;
         }
     }
+}
+
+// mbar_wait for every lane of a warp whose next steps are warp-collective (tcgen05.ld/st,
+// shuffles, votes): the warp goes on only if every lane saw the phase complete, so a limit
+// that runs out in some lanes and not in others cannot split the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                               uint64_t limit_ns) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status, limit_ns));
 }
 
 // Bounded wait that ignores the abort flag: used while winding down to let copies or

@@ -23,6 +23,7 @@ EXPORTS = (
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
     "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward", "lin_attn_forward_fused_layout",
+    "lin_attn_set_wait_limit",
 )
 
 
@@ -41,6 +42,7 @@ def _load():
         "lin_attn_device_status": ([p, p], i32),
         "lin_attn_kv_plan": ([i32, i64, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "lin_attn_set_stage_events": ([p, ctypes.POINTER(p), i32], i32),
+        "lin_attn_set_wait_limit": ([p, ctypes.c_uint64], i32),
         "lin_attn_error_string": ([i32], ctypes.c_char_p),
         "lin_attn_last_error": ([], ctypes.c_char_p),
         "lin_attn_version": ([], i32),
@@ -105,8 +107,8 @@ def _stream_handle(stream, device) -> int:
 
 
 def forward_noalloc(q_rot, k_rot, v, normalizer, out, mode="high", stream=None):
-    """Layer call that allocates no device memory (library-owned fixed scratch, current
-    device); for callers that cannot allocate.  ``out`` must be given."""
+    """Layer call that allocates no device memory (library-owned fixed scratch on the
+    inputs' device); for callers that cannot allocate.  ``out`` must be given."""
     for name, t in (("q_rot", q_rot), ("k_rot", k_rot), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
@@ -117,9 +119,16 @@ def forward_noalloc(q_rot, k_rot, v, normalizer, out, mode="high", stream=None):
         raise ValueError(f"normalizer must be a contiguous float32 [1, {H}, {N}, 1] tensor")
     if out.shape != q_rot.shape or not out.is_contiguous():
         raise ValueError("out must be a contiguous [1, H, N, D] tensor")
-    st = lib.lin_attn_forward_noalloc(q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(),
-                                      out.data_ptr(), _out_code(out.dtype), H, N, D, _mode(mode),
-                                      _stream_handle(stream, q_rot.device))
+    code = _out_code(out.dtype)
+    dev = q_rot.device
+    for name, t in (("k_rot", k_rot), ("v", v), ("normalizer", normalizer), ("out", out)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}; every tensor must be on {dev}")
+    # The entry point runs on the calling thread's current device (its scratch, set-up and
+    # the stream all belong to it): make that the tensors' device for the call.
+    with torch.cuda.device(dev):
+        st = lib.lin_attn_forward_noalloc(q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), normalizer.data_ptr(),
+                                          out.data_ptr(), code, H, N, D, _mode(mode), _stream_handle(stream, dev))
     _check(st, "lin_attn_forward_noalloc")
     return out
 
@@ -269,6 +278,10 @@ class LinAttn:
     def device_status(self, stream=None) -> int:
         """Synchronise the stream and return (clearing) the kernels' status word."""
         return lib.lin_attn_device_status(self._h, _stream_handle(stream, self.device))
+
+    def set_wait_limit(self, limit_ns: int):
+        """Test hook: barrier-wait limit of the kernels of later calls (0 = the 2 s default)."""
+        _check(lib.lin_attn_set_wait_limit(self._h, int(limit_ns)), "lin_attn_set_wait_limit")
 
     def set_stage_events(self, events):
         """Arm 4 timing events (torch.cuda.Event(enable_timing=True)) for the next forward."""
