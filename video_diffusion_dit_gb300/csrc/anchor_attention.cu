@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            if (!(ok = mbar_wait_warp(s_full0 + 8u * t, j & 1u, abort_flag, status, wait_ns))) break;
+            if (!(ok = mbar_wait(s_full0 + 8u * t, j & 1u, abort_flag, status, wait_ns))) break;
             tc_fence_after();
             // The whole row of S_t(j); keys past the end are masked out.
             const int valid = min(kBN, n_tokens - j * kBN);
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_arrive(p_full0 + 8u * t);
         }
         // Epilogue: O_t / l once the last product has landed.
-        if (ok && mbar_wait_warp(o_done, 0, abort_flag, status, wait_ns)) {
+        if (ok && mbar_wait(o_done, 0, abort_flag, status, wait_ns)) {
             tc_fence_after();
             const int row = m0 + kBM * t + r;
             const float inv = 1.0f / l;

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             const uint32_t buf = lt & 1u;
             const float dv = row < n_tokens ? den[static_cast<int64_t>(h) * n_tokens + row] : 1.0f;
             const float rcp = __frcp_rn(dv);
-            if (!mbar_wait_warp(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns)) break;
+            if (!mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
             // A warp whose 32 rows all lie past the end of the head (ragged last tile) has

@@ -285,15 +285,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
             const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
-            if (!mbar_wait_warp(q_full0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
-            if (!mbar_wait_warp(den_empty0 + 8u * db, dph ^ 1u, abort_flag, status, wait_ns)) break;
+            if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
+            if (!mbar_wait(den_empty0 + 8u * db, dph ^ 1u, abort_flag, status, wait_ns)) break;
             uint8_t* atom = base_ptr + (q_smem - base) + (st * NBOX + (c >> 3)) * kFQAtom;
             bool ok = true;
 #pragma unroll
             for (int hh = 0; hh < kFTabSubs; ++hh) {
                 const uint32_t i = kFTabSubs * it + hh;
                 const uint32_t slot = i % kFTabSlots;
-                if (!(ok = mbar_wait_warp(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status, wait_ns))) break;
+                if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status, wait_ns))) break;
                 const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;
                 constexpr int kPer = kFTabRows / kFRowGroups;  // this thread's rows per slot
 #pragma unroll
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (cur_h < 0) grid_dependency_wait();
                 ++run;
                 cur_h = h;
-                if (run > 0 && !(ok = mbar_wait_warp(b_empty, (run - 1) & 1, abort_flag, status, wait_ns))) break;
+                if (run > 0 && !(ok = mbar_wait(b_empty, (run - 1) & 1, abort_flag, status, wait_ns))) break;
                 tc_fence_after();
                 const uint8_t* img = kv_image + static_cast<int64_t>(h) * 3 * term_bytes;
                 const uint32_t groups = 3u * half_d / 8u;  // 8-word groups of the three terms
@@ -389,8 +389,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             const uint32_t buf = lt & 1u;
             const uint32_t db = lt % kFDenBufs, dph = (lt / kFDenBufs) & 1u;
-            if (!(ok = mbar_wait_warp(den_full0 + 8u * db, dph, abort_flag, status, wait_ns))) break;
-            if (!(ok = mbar_wait_warp(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns))) break;
+            if (!(ok = mbar_wait(den_full0 + 8u * db, dph, abort_flag, status, wait_ns))) break;
+            if (!(ok = mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns))) break;
             tc_fence_after();
             const float* rcp_t = rcp_s + db * kApplyTile;
             for (int g = 2 * e; g < 2 * e + 2 && n0 + 32 * g < n_tokens; ++g) {

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             for (int e = 0; e < 4; ++e) ks[e] = kc[e] = 0ull;
             for (; t < seg_end; ++t, ++it) {
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
-                if (!mbar_wait_warp(full0 + 8u * st, ph, abort_flag, status, wait_ns)) {
+                if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             }
             for (int64_t k0 = t; k0 < seg_end; k0 += PROMOTE, ++sub) {
                 const uint32_t buf = sub & 1u;
-                if (!mbar_wait_warp(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status, wait_ns)) {
+                if (!mbar_wait(acc_full0 + 8u * buf, (sub >> 1) & 1u, abort_flag, status, wait_ns)) {
                     ok = false;
                     break;
                 }

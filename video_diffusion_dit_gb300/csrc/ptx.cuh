@@ -68,6 +68,10 @@ constexpr uint64_t kBlockingProbeMinNs = 1000000ull;  // 1 ms
 // Wait for the phase with the given parity to complete.  Returns false (without the
 // phase completing) if the CTA's abort flag is raised or `limit_ns` passes; in the latter
 // case it raises the abort flag and records a timeout in the status word.
+// Warps whose next step is warp-collective (tcgen05.ld/st, shuffles) call this with all
+// lanes, entering converged: every exit test reads the same barrier word, the same timer
+// value and the same abort flag in the same instruction for all lanes, so the lanes leave
+// together and the warp is not split before the collective step.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                           uint64_t limit_ns) {
     const bool poll = limit_ns < kBlockingProbeMinNs;
@@ -82,14 +86,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             return false;
         }
     }
-}
-
-// mbar_wait for every lane of a warp whose next steps are warp-collective (tcgen05.ld/st,
-// shuffles, votes): the warp goes on only if every lane saw the phase complete, so a limit
-// that runs out in some lanes and not in others cannot split the warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                               uint64_t limit_ns) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status, limit_ns));
 }
 
 // Bounded wait that ignores the abort flag: used while winding down to let copies or
