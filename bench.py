@@ -78,24 +78,37 @@ def anchor_flops(H, N, D):
 
 
 def kernel_traffic(kernel, config, path=None):
-    """DRAM bytes per launch from the committed ncu capture, or None when the capture was
-    of another configuration (workload, tier, output type, layout, producer), the kernel
-    source changed since the capture, or no capture exists."""
+    """DRAM bytes per launch from the committed ncu captures, or None when no capture is of
+    this configuration (workload, tier, output type, layout, producer), the kernel source
+    changed since the capture, or no capture exists."""
     p = path or os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get("kernels", {}).get(kernel)
-    if not ent or d.get("config") != config:
-        return None
-    src = os.path.join(ROOT, ent["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != ent["source_sha256"]:
+    for cap in d.get("captures", []):
+        ent = cap.get("kernels", {}).get(kernel)
+        if not ent or cap.get("config") != config:
+            continue
+        digest = sources_sha256(ent["sources"])
+        if digest is None or digest != ent["sources_sha256"]:
             return None
-    return ent.get("bytes_per_launch_full")
+        return ent.get("bytes_per_launch_full")
+    return None
+
+
+def sources_sha256(paths):
+    """SHA-256 over the given source files (repo-relative), concatenated in order; None if
+    one is missing.  The traffic captures pin the kernel's .cu file and the headers it
+    includes, so any edit to the code the counters belong to retires them."""
+    h = hashlib.sha256()
+    for rel in paths:
+        p = os.path.join(ROOT, rel)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:

@@ -208,8 +208,8 @@ int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *ma
  * are LIN_ATTN_ERR_INVALID_ARG).  A kernel that gives up winds down cleanly - it lets its
  * copies and tensor-core operations in flight land, frees its tensor memory and exits -
  * and records LIN_ATTN_ERR_TIMEOUT for lin_attn_device_status; that call's output is then
- * incomplete.  Limits below 1 ms are checked with non-blocking barrier probes, so a wait
- * that is not already over when it starts gives up within about the limit.  Used to show
+ * incomplete.  With a limit below 1 ms, a wait that outlasts its first (blocking) probe is
+ * then checked with non-blocking probes and gives up within about the limit.  Used to show
  * that the bounded waits report instead of hanging; calls made with the default limit are
  * unaffected.
  */

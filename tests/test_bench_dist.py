@@ -63,29 +63,36 @@ def test_reference_arm_under_torchrun_prints_once():
 
 
 def test_traffic_is_reported_only_for_the_captured_configuration(tmp_path):
-    # The committed ncu byte counts belong to one configuration and one kernel source;
-    # any other configuration, or an edited source, reports null rather than a stale count.
-    import hashlib
+    # The committed ncu byte counts belong to one configuration and one version of the kernel
+    # sources; any other configuration, or an edited source, reports null rather than a
+    # stale count.
     sys.path.insert(0, ROOT)
     import bench
-    with open(os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")) as f:
-        cap = json.load(f)
-    cfg = dict(cap["config"])
-    for ent in cap["kernels"].values():  # the same file, with the sources as they are now
-        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
-            ent["source_sha256"] = hashlib.sha256(f.read()).hexdigest()
+    srcs = ["video_diffusion_dit_gb300/csrc/apply.cu", "video_diffusion_dit_gb300/csrc/ptx.cuh",
+            "video_diffusion_dit_gb300/csrc/lin_attn_internal.cuh"]
+    cfg = {"workload": "720p_193f", "mode": "high", "out_dtype": "f32", "layout": "hnd", "fused": False}
+    cap = {"captures": [
+        {"config": cfg, "kernels": {"apply_tc_kernel": {"sources": srcs, "sources_sha256": bench.sources_sha256(srcs),
+                                                         "bytes_per_launch_full": 123}}},
+        {"config": {**cfg, "layout": "nhd"},
+         "kernels": {"apply_tc_kernel": {"sources": srcs, "sources_sha256": bench.sources_sha256(srcs),
+                                         "bytes_per_launch_full": 456}}},
+    ]}
     cur = tmp_path / "current.json"
     cur.write_text(json.dumps(cap))
-    for kernel, ent in cap["kernels"].items():
-        assert bench.kernel_traffic(kernel, cfg, str(cur)) == ent["bytes_per_launch_full"]
-        for key, other in (("workload", "480p_81f"), ("mode", "lossless"), ("out_dtype", "bf16"),
-                           ("layout", "nhd"), ("fused", True)):
-            assert bench.kernel_traffic(kernel, {**cfg, key: other}, str(cur)) is None
+    assert bench.kernel_traffic("apply_tc_kernel", cfg, str(cur)) == 123
+    assert bench.kernel_traffic("apply_tc_kernel", {**cfg, "layout": "nhd"}, str(cur)) == 456
+    for key, other in (("workload", "480p_81f"), ("mode", "lossless"), ("out_dtype", "bf16"), ("fused", True)):
+        assert bench.kernel_traffic("apply_tc_kernel", {**cfg, key: other}, str(cur)) is None
     assert bench.kernel_traffic("apply_fused_kernel", cfg, str(cur)) is None
-    stale = json.loads(cur.read_text())
-    for ent in stale["kernels"].values():
-        ent["source_sha256"] = "0" * 64
+    for c in cap["captures"]:
+        c["kernels"]["apply_tc_kernel"]["sources_sha256"] = "0" * 64
     old = tmp_path / "stale.json"
-    old.write_text(json.dumps(stale))
-    for kernel in stale["kernels"]:
-        assert bench.kernel_traffic(kernel, cfg, str(old)) is None
+    old.write_text(json.dumps(cap))
+    assert bench.kernel_traffic("apply_tc_kernel", cfg, str(old)) is None
+    # The committed captures parse, and each names sources that exist.
+    with open(os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")) as f:
+        committed = json.load(f)
+    for c in committed["captures"]:
+        for ent in c["kernels"].values():
+            assert bench.sources_sha256(ent["sources"]) is not None

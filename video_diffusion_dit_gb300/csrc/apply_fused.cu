@@ -13,8 +13,8 @@
 // The KV image (KV^T split into three BF16 terms hi + mid + lo, which carry 24 bits of KV,
 // so every product is exact in FP32 and the result has FP32-class accuracy) lives in TMEM
 // as the A operand of tcgen05.mma, which leaves shared memory to the streams: Q tiles, the
-// rotation-table rows and the output staging.  Per CTA (persistent, contiguous ranges of
-// the (head, tile) sequence):
+// rotation-table rows and the output staging.  Per CTA (persistent; k CTAs per head, each
+// a contiguous range of one head's tiles, every head cut at the same tiles):
 //   warp 0      TMA Q tiles (K-major, 128-byte swizzle: the B operand as loaded) and
 //               bulk-copies each half tile's table rows into a three-slot ring;
 //   warp 1      3 terms x D/16 K-steps of tcgen05.mma M=128 (features) N=128 (tokens) into
@@ -111,19 +111,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Head-major activations: contiguous ranges of the layer's (head, tile) sequence.
-    // Token-major: gridDim = k heads, CTA b takes part b % k of head b / k, every head cut
-    // at the same tiles, so the CTAs running together read and write the same token rows.
-    int t_begin, t_end;
-    if (!token_major) {
-        const int total = heads * tiles_per_head;
-        t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-        t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
-    } else {
-        const int k = gridDim.x / heads, hb = blockIdx.x / k, g = blockIdx.x % k;
-        t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k);
-        t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k);
-    }
+    // gridDim = k heads: CTA b takes part b % k of head b / k, every head cut at the same
+    // tiles, so the CTAs running together work on the same token rows.  They then read each
+    // rotation-table row (the same for every head) from DRAM once, and token-major
+    // activations on whole DRAM rows.  (Contiguous ranges of the (head, tile) sequence keep
+    // all 152 SMs busy, but the CTAs then walk the whole token range at once and the 80 MB of
+    // tables at 720p were read from DRAM about five times: 0.8 % slower per call.)
+    const int k_per_head = gridDim.x / heads, hb = blockIdx.x / k_per_head, g = blockIdx.x % k_per_head;
+    const int t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k_per_head);
+    const int t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k_per_head);
     const uint32_t half_d = static_cast<uint32_t>(head_dim / 2);  // image columns per term
 
     if (threadIdx.x == 0) {
@@ -467,7 +463,7 @@ cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm
     const int tph = (n + kApplyTile - 1) / kApplyTile;
     const int total = heads * tph;
     if (grid > total) grid = total;
-    if (token_major) {  // a whole number of CTAs per head (see the kernel's schedule)
+    {  // a whole number of CTAs per head (see the kernel's schedule)
         const int k = grid / heads < 1 ? 1 : (grid / heads < tph ? grid / heads : tph);
         grid = k * heads;
     }

@@ -61,8 +61,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Limits below this are probed with the non-blocking test_wait, so that the limit itself -
-// not the hardware's own suspend window inside try_wait - decides when a wait gives up.
+// Once a wait has outlasted its first (blocking) probe, limits below this are probed with
+// the non-blocking test_wait, so that the limit itself - not the hardware's own suspend
+// window inside try_wait - decides when the wait gives up.  The first probe is always
+// try_wait: a branch on the limit there cost the softmax anchor kernel about 2 %.
 constexpr uint64_t kBlockingProbeMinNs = 1000000ull;  // 1 ms
 
 // Wait for the phase with the given parity to complete.  Returns false (without the
@@ -74,8 +76,8 @@ constexpr uint64_t kBlockingProbeMinNs = 1000000ull;  // 1 ms
 // together and the warp is not split before the collective step.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                           uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
     const bool poll = limit_ns < kBlockingProbeMinNs;
-    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
