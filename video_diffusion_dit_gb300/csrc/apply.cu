@@ -47,7 +47,7 @@ static_assert(apply_smem_bytes(128) <= kSmemLimit && apply_smem_bytes(64) <= kSm
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kApplyThreads, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
-                    const uint8_t* __restrict__ kv_image, const float* __restrict__ den, int heads, int n_tokens,
+                    const uint8_t* kv_image, const float* __restrict__ den, int heads, int n_tokens,
                     int head_dim, int tiles_per_head, int token_major, int* status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);

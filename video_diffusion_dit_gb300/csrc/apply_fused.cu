@@ -78,7 +78,7 @@ static_assert(kFTabRows % (kFXfWarps * 32 / 16) == 0, "a table slot must hold wh
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
     apply_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
-                       const uint8_t* __restrict__ kv_image, int heads, int n_tokens, int head_dim,
+                       const uint8_t* kv_image, int heads, int n_tokens, int head_dim,
                        int tiles_per_head, int token_major, int* status, uint64_t wait_ns,
                        const ProducerArgs pa) {
     constexpr int kStages = fused_stages(NBOX);

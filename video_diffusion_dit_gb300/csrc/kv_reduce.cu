@@ -431,10 +431,6 @@ __device__ __forceinline__ float reduce_segments(const float* p, int64_t stride,
     return pairwise_sum(groups, ngroups);
 }
 
-// A CTA reduces an 8-row x 32-column tile of one head's KV: thread (row e, column jl)
-// adds the partials of one element (loads coalesced across the 32 columns), then the
-// tile goes through shared memory so that 32 threads each write one 16-byte chunk (8
-// consecutive rows i of column j) per term of the image.
 // Fixed-order sum of a head's FP64 column-sum partials (fused path): each segment's value
 // is its row-group sums added in order (p[s][0..kKsumGroups-1], `stride` apart), then the
 // segments are added with the same tree as above.
@@ -473,44 +469,95 @@ __device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t s
     return groups[0];
 }
 
-__global__ void __launch_bounds__(256) kv_finalize_kernel(const float* __restrict__ partial,
-                                                          float* __restrict__ kv, uint8_t* __restrict__ image,
-                                                          int h0, int head_dim, const KvPlan plan,
-                                                          const double* __restrict__ ksum_partial,
-                                                          float* __restrict__ ksum) {
+// One CTA per 8-row slab of one head's KV (all D columns): thread (row e, column lane jl)
+// takes the elements (8r + e, jl + 32 cb).  With at most kSmallSegs partials per head
+// (every head count from 10 up) all of a thread's loads are issued before any add, so a
+// slab costs one round trip to L2 and the reduction is a single wave of D/8 x H CTAs;
+// with more partials each element goes through reduce_segments in turn.  The partials of
+// an element are added in the same fixed pairwise order either way (pairwise_sum over 16
+// values performs the same additions as over 32 when at most 16 are present).
+constexpr int kSmallSegs = 16;
+constexpr int kColBlocks = 4;  // 32-column blocks: head_dim <= 128
+
+// The partials (and column-sum partials) are written by the kernel before this one in the
+// stream, which may still be running when this grid starts: they are read through plain
+// pointers, never `__restrict__` ones, so that no load of them can be treated as invariant
+// and moved above the grid-dependency wait.
+template <bool SMALL>
+__global__ void __launch_bounds__(256, 2) kv_finalize_kernel(const float* partial, float* __restrict__ kv,
+                                                             uint8_t* __restrict__ image, int h0, int head_dim,
+                                                             const KvPlan plan, const double* ksum_partial,
+                                                             float* __restrict__ ksum) {
     grid_launch_dependents();  // the apply kernel may start its prologue and Q loads now
     grid_dependency_wait();    // the partials of this call are complete past this point
-    __shared__ float tile[8][33];
-    const int h = h0 + blockIdx.z;
+    __shared__ float tile[kColBlocks][8][33];
+    __shared__ double ks_seg[kSmallSegs][8];
+    const int h = h0 + blockIdx.y;
     const int dd = head_dim * head_dim;
-    const int r = blockIdx.y;                // rows 8r .. 8r+7
-    const int j0 = blockIdx.x * 32;          // columns j0 .. j0+31
+    const int r = blockIdx.x;  // rows 8r .. 8r+7
     const int e = threadIdx.x >> 5, jl = threadIdx.x & 31;
-    const int i = 8 * r + e, j = j0 + jl;
+    const int i = 8 * r + e;
+    const int ncb = (head_dim + 31) / 32;
     const int nseg = segments_of_head(plan, h);
-    if (ksum_partial != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < head_dim) {
-        // Fused path: column sums of relu(K) over all tokens, rounded once to FP32.
-        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * kKsumGroups * head_dim + threadIdx.x;
-        ksum[h * head_dim + threadIdx.x] = static_cast<float>(reduce_segments_f64(kp, head_dim, nseg));
+    const float* p = partial + static_cast<int64_t>(h) * plan.seg_stride * dd + i * head_dim + jl;
+    float* kv_row = kv + static_cast<int64_t>(h) * dd + i * head_dim + jl;
+    if constexpr (SMALL) {
+        float v[kColBlocks][kSmallSegs];
+#pragma unroll
+        for (int cb = 0; cb < kColBlocks; ++cb)
+#pragma unroll
+            for (int sg = 0; sg < kSmallSegs; ++sg)
+                v[cb][sg] = (cb < ncb && jl + 32 * cb < head_dim && sg < nseg) ? p[sg * dd + 32 * cb] : 0.f;
+#pragma unroll
+        for (int cb = 0; cb < kColBlocks; ++cb) {
+            const float x = pairwise_sum(v[cb], nseg);
+            if (cb < ncb && jl + 32 * cb < head_dim) kv_row[32 * cb] = x;
+            tile[cb][e][jl] = x;
+        }
+    } else {
+#pragma unroll 1
+        for (int cb = 0; cb < ncb; ++cb) {
+            const float x = jl + 32 * cb < head_dim ? reduce_segments(p + 32 * cb, dd, nseg) : 0.f;
+            if (jl + 32 * cb < head_dim) kv_row[32 * cb] = x;
+            tile[cb][e][jl] = x;
+        }
     }
-    float x = 0.f;
-    if (j < head_dim) {
-        const float* p = partial + static_cast<int64_t>(h) * plan.seg_stride * dd + i * head_dim + j;
-        x = reduce_segments(p, dd, nseg);
-        kv[static_cast<int64_t>(h) * dd + i * head_dim + j] = x;
+    if (ksum_partial != nullptr) {
+        // Fused path: the column sums of relu(K) of columns 8r .. 8r+7 over all tokens, each
+        // segment's row groups in order, then the segments in the same tree; rounded once to FP32.
+        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * kKsumGroups * head_dim;
+        const int t = threadIdx.x;
+        if constexpr (SMALL) {
+            if (t < 8 * nseg) ks_seg[t >> 3][t & 7] = segment_value_f64(kp + 8 * r + (t & 7), head_dim, t >> 3);
+            __syncthreads();
+            if (t < 8) {
+                double vals[kSmallSegs];
+#pragma unroll
+                for (int sg = 0; sg < kSmallSegs; ++sg) vals[sg] = sg < nseg ? ks_seg[sg][t] : 0.0;
+#pragma unroll
+                for (int w = 1; w < kSmallSegs; w *= 2)
+#pragma unroll
+                    for (int sg = 0; sg + w < kSmallSegs; sg += 2 * w)
+                        if (sg + w < nseg) vals[sg] = vals[sg] + vals[sg + w];
+                ksum[h * head_dim + 8 * r + t] = static_cast<float>(vals[0]);
+            }
+        } else if (t < 8) {
+            ksum[h * head_dim + 8 * r + t] = static_cast<float>(reduce_segments_f64(kp + 8 * r + t, head_dim, nseg));
+        }
     }
     if (image == nullptr) return;
-    tile[e][jl] = x;
     __syncthreads();
-    if (threadIdx.x >= 32 || j0 + threadIdx.x >= head_dim) return;
-    const int jj = j0 + threadIdx.x;
+    // The image: 32 threads per column block each write one 16-byte chunk (8 consecutive
+    // rows i of column jj) per term.
+    const int cb = threadIdx.x >> 5, jj = 32 * cb + jl;
+    if (cb >= ncb || jj >= head_dim) return;
     uint32_t hi[4], mid[4], lo[4];
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
         __nv_bfloat16 h2[2], m2[2], l2[2];
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-            const float v = tile[u + w][threadIdx.x];
+            const float v = tile[cb][u + w][jl];
             h2[w] = __float2bfloat16_rn(v);
             const float r1 = v - __bfloat162float(h2[w]);  // exact
             m2[w] = __float2bfloat16_rn(r1);
@@ -571,10 +618,13 @@ cudaError_t launch_kv_partial_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_
 
 cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_image, int h0, int hc, int head_dim,
                                const KvPlan& plan, cudaStream_t stream, const ProducerArgs* producer) {
-    dim3 grid((head_dim + 31) / 32, head_dim / 8, hc);
+    dim3 grid(head_dim / 8, hc);
     const double* kp = producer ? producer->ksum_partial : nullptr;
     float* ks = producer ? producer->ksum : nullptr;
-    return launch_overlapped(kv_finalize_kernel, grid, dim3(256), 0, stream, partial, kv, kv_image, h0, head_dim,
+    if (plan.per_head <= kSmallSegs)
+        return launch_overlapped(kv_finalize_kernel<true>, grid, dim3(256), 0, stream, partial, kv, kv_image, h0,
+                                 head_dim, plan, kp, ks);
+    return launch_overlapped(kv_finalize_kernel<false>, grid, dim3(256), 0, stream, partial, kv, kv_image, h0, head_dim,
                              plan, kp, ks);
 }
 
