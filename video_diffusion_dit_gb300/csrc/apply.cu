@@ -22,13 +22,18 @@ namespace {
 // layout) and, when the head changes, bulk-copies that head's KV image (three BF16 terms
 // KV = hi + mid + lo, already in the swizzled K-major B layout) into shared memory.
 // Warp 1 issues, per tile, 3 terms x (Dpad / 16) MMAs of 128 x D x 16 into one of two TMEM
-// accumulators.  Warps 2..5 read the accumulator (one token row per thread), multiply by
-// the reciprocal denominator and write 32-row boxes through swizzled staging with TMA
-// stores.  BF16 x BF16 products are exact in FP32 and the three terms carry 24 bits of
+// accumulators.  Warps 2..9 read the accumulator (one token row per thread; two warps per
+// TMEM lane quarter, each with half of the tile's column groups), multiply by the
+// reciprocal denominator and write 32-row boxes through swizzled staging with TMA stores.  BF16 x BF16 products are exact in FP32 and the three terms carry 24 bits of
 // KV, so the result has FP32-class accuracy (the tier's second GEMM "stays FP32").
-constexpr int kApplyThreads = 192;
+// Epilogue: two warps per TMEM lane quarter, each taking half of a tile's column groups,
+// with two staging buffers each when the head dim fits one 64-column atom and one
+// otherwise (the 86 KB KV image leaves room for no more).
+constexpr int kApplyEpiWarps = 8;
+constexpr int kApplyThreads = 32 * (2 + kApplyEpiWarps);
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
 constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
+__host__ __device__ constexpr uint32_t apply_out_bufs(int nbox) { return nbox == 1 ? 2u : 1u; }
 constexpr uint32_t kApplyBarBytes = 512;            // mbarriers, TMEM address, abort flag
 constexpr uint32_t kSmemLimit = 232448;
 
@@ -38,8 +43,8 @@ __host__ __device__ constexpr int apply_stages(int nbox) { return nbox == 1 ? 6 
 
 __host__ __device__ constexpr uint32_t apply_smem_bytes(int head_dim) {
     return static_cast<uint32_t>(kv_image_bytes(head_dim)) +
-           apply_stages(head_dim_atoms(head_dim)) * head_dim_atoms(head_dim) * kQAtomBytes + 4 * 2 * kOutBoxBytes +
-           kApplyBarBytes + 1024;
+           apply_stages(head_dim_atoms(head_dim)) * head_dim_atoms(head_dim) * kQAtomBytes +
+           kApplyEpiWarps * apply_out_bufs(head_dim_atoms(head_dim)) * kOutBoxBytes + kApplyBarBytes + 1024;
 }
 static_assert(apply_smem_bytes(128) <= kSmemLimit && apply_smem_bytes(64) <= kSmemLimit,
               "apply layout exceeds shared memory");
@@ -60,7 +65,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
     const uint32_t b_smem = base;
     const uint32_t q_smem = b_smem + img_bytes;
     const uint32_t o_smem = q_smem + kApplyStages * NBOX * kQAtomBytes;
-    const uint32_t bar_off = o_smem + 4 * 2 * kOutBoxBytes - base;
+    constexpr uint32_t kOutBufs = apply_out_bufs(NBOX);
+    const uint32_t bar_off = o_smem + kApplyEpiWarps * kOutBufs * kOutBoxBytes - base;
     const uint32_t bars = base + bar_off;
     const uint32_t q_full0 = bars;                        // [kApplyStages]
     const uint32_t q_empty0 = bars + 8u * kApplyStages;   // [kApplyStages]
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
-            mbar_init(acc_empty0 + 8u * b, 4);
+            mbar_init(acc_empty0 + 8u * b, kApplyEpiWarps);
         }
         mbar_init(b_full, 1);
         mbar_init(b_empty, 1);
@@ -210,15 +216,19 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             mbar_wait_drain(drain_bar, 0);
         }
     } else {
-        // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes / tile rows 32q..32q+31
+        // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes / tile rows 32q..32q+31,
+        // half eh = (warp - 2) / 4 of the column groups
         const int q = warp & 3;
-        const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
+        const int eh = (warp - 2) >> 2;
+        const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * kOutBufs * kOutBoxBytes;
         uint32_t nstore = 0;
         // Token-major output rows share L2 lines with the neighbouring heads' rows (written by
         // other CTAs): normal priority, as for the loads.
         const uint64_t spol = token_major ? policy_evict_normal() : policy_evict_first();
         constexpr int kCols = OUT_BF16 ? 64 : 32;  // columns per 128-byte box row
         const int groups = (head_dim + kCols - 1) / kCols;
+        const int g_per = (groups + 1) / 2;
+        const int g_lo = eh * g_per, g_hi = min(groups, g_lo + g_per);
         for (int t = t_begin; t < t_end; ++t) {
             const int h = t / tiles_per_head;
             const int n0 = (t % tiles_per_head) * kApplyTile;
@@ -235,8 +245,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             // nothing to store.  It must not touch its staging buffers either: every buffer
             // write is paired with one committed store, which is what lets wait_group.read 1
             // guarantee the buffer's previous store has finished reading it.
-            const int live_groups = row0 < n_tokens ? groups : 0;
-            for (int g = 0; g < live_groups; ++g) {
+            const int live_hi = row0 < n_tokens ? g_hi : g_lo;
+            for (int g = g_lo; g < live_hi; ++g) {
                 uint32_t packed[32];
                 if (!OUT_BF16) {
                     uint32_t r[32];
@@ -256,8 +266,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                         }
                     }
                 }
-                const uint32_t sbuf = stage0 + (nstore & 1u) * kOutBoxBytes;
-                if (lane == 0) bulk_wait_read<1>();
+                const uint32_t sbuf = stage0 + (nstore % kOutBufs) * kOutBoxBytes;
+                if (lane == 0) bulk_wait_read<kOutBufs - 1>();
                 __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
