@@ -24,11 +24,11 @@ namespace {
 // Warp 1 issues, per tile, 3 terms x (Dpad / 16) MMAs of 128 x D x 16 into one of two TMEM
 // accumulators.  Warps 2..9 read the accumulator (one token row per thread; two warps per
 // TMEM lane quarter, each with half of the tile's column groups), multiply by the
-// reciprocal denominator and write 32-row boxes through swizzled staging with TMA stores.  BF16 x BF16 products are exact in FP32 and the three terms carry 24 bits of
-// KV, so the result has FP32-class accuracy (the tier's second GEMM "stays FP32").
-// Epilogue: two warps per TMEM lane quarter, each taking half of a tile's column groups,
-// with two staging buffers each when the head dim fits one 64-column atom and one
-// otherwise (the 86 KB KV image leaves room for no more).
+// reciprocal denominator and write 32-row boxes through swizzled staging with TMA stores:
+// two staging buffers per warp when the head dim fits one 64-column atom, one otherwise
+// (the 86 KB KV image leaves room for no more).  BF16 x BF16 products are exact in FP32 and
+// the three terms carry 24 bits of KV, so the result has FP32-class accuracy (the tier's
+// second GEMM "stays FP32").
 constexpr int kApplyEpiWarps = 8;
 constexpr int kApplyThreads = 32 * (2 + kApplyEpiWarps);
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes

@@ -32,6 +32,8 @@ constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
 constexpr int kKvThreadsFused = 192 + 32 * kKsumGroups / 2;  // + warps 6..13: the producer-step transform
 constexpr int kKvTransformThreads = kKvThreadsFused - 192;
+static_assert(kKvTransformThreads == 16 * kKsumGroups && kKvTile % kKsumGroups == 0,
+              "transform thread (chunk, row group) covers rows rg + kKsumGroups k of every tile");
 // Tiles per tensor-core sub-chunk before its sum is promoted into FP32 registers: 4 (256
 // tokens) in the 'high' tier, 1 (64 tokens) in the 'lossless' tier.
 constexpr int kPromoteHigh = 4;
@@ -249,15 +251,17 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     break;
                 }
                 if (live) {
-                    const int n0 = static_cast<int>((t % tph) * kKvTile);
+                    // Rows past the end of the sequence hold zeros in both the K and the table
+                    // tiles (the copies fill outside the tensor with zeros): they rotate to zero
+                    // and add zero to the sums, so every row is transformed without a test.
                     uint8_t* stage = base_ptr + st * L::stage_bytes;
                     uint8_t* atom = stage + (c >> 3) * kKvAtomBytes;
                     const uint8_t* tab = stage + L::a_bytes + L::b_bytes + 16 * c;  // [64][pairs] floats
                     uint64_t ts[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int k = 0; k < (kKvTile + kKsumGroups - 1) / kKsumGroups; ++k) {
+                    for (int k = 0; k < kKvTile / kKsumGroups; ++k) {
                         const int r = rg + kKsumGroups * k;
-                        if (r < kKvTile && n0 + r < pa.n_tokens) {  // rows past the end stay zero
+                        {
                             uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                             uint4 w = *cell;
                             const float4 c4 = *reinterpret_cast<const float4*>(tab + r * pairs * 4);
