@@ -292,33 +292,52 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status, wait_ns))) break;
                 const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;
                 constexpr int kPer = kFTabRows / kFRowGroups;  // this thread's rows per slot
+                float part[kPer];
+                if (live) {
+                    // All of the slot's loads first, then the arithmetic: the rows' chains overlap.
+                    // Rows past the end of the sequence are not tested for: their Q is zero (the
+                    // copy fills outside the tensor with zeros), so their normaliser is the
+                    // constant; their table rows were not copied, so what they compute is never
+                    // used - an output column depends on its own token's row only, and the
+                    // stores stop at N.
+                    uint4* cell[kPer];
+                    uint4 w[kPer];
+                    float4 c4[kPer], s4[kPer];
 #pragma unroll
-                for (int k = kPer * hh; k < kPer * hh + kPer; ++k) {
-                    const int r = rg + kFRowGroups * k;
-                    const int n = n0 + r;
-                    float part = 0.f;
-                    if (live && n < n_tokens) {
+                    for (int kk = 0; kk < kPer; ++kk) {
+                        const int r = rg + kFRowGroups * (kPer * hh + kk);
                         const uint32_t tr = static_cast<uint32_t>(r - hh * kFTabRows) * row_bytes;
-                        const float4 c4 = *reinterpret_cast<const float4*>(tab + tr);
-                        const float4 s4 = *reinterpret_cast<const float4*>(tab + tab_slot / 2 + tr);
-                        uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-                        uint4 w = *cell;
+                        cell[kk] = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                        w[kk] = *cell[kk];
+                        c4[kk] = *reinterpret_cast<const float4*>(tab + tr);
+                        s4[kk] = *reinterpret_cast<const float4*>(tab + tab_slot / 2 + tr);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kPer; ++kk) {
                         uint64_t a0[2], a1[2];
-                        rope_chunk(w, c4, s4, a0, a1);
+                        rope_chunk(w[kk], c4[kk], s4[kk], a0, a1);
                         uint64_t d2 = f32x2_mul(a0[0], ks[0]);
                         d2 = f32x2_fma(a0[1], ks[1], d2);
                         d2 = f32x2_fma(a1[0], ks[2], d2);
                         d2 = f32x2_fma(a1[1], ks[3], d2);
                         float d0, d1;
                         f32x2_unpack(d2, d0, d1);
-                        part = d0 + d1;
-                        *cell = w;
+                        part[kk] = d0 + d1;
+                        *cell[kk] = w[kk];
                     }
-                    part += __shfl_xor_sync(0xffffffffu, part, 8);
-                    part += __shfl_xor_sync(0xffffffffu, part, 4);
-                    part += __shfl_xor_sync(0xffffffffu, part, 2);
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    if (c == 0) rcp_s[db * kApplyTile + r] = __frcp_rn(part + kDenEps);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kPer; ++kk) part[kk] = 0.f;
+                }
+#pragma unroll
+                for (int kk = 0; kk < kPer; ++kk) {
+                    const int r = rg + kFRowGroups * (kPer * hh + kk);
+                    float p = part[kk];
+                    p += __shfl_xor_sync(0xffffffffu, p, 8);
+                    p += __shfl_xor_sync(0xffffffffu, p, 4);
+                    p += __shfl_xor_sync(0xffffffffu, p, 2);
+                    p += __shfl_xor_sync(0xffffffffu, p, 1);
+                    if (c == 0) rcp_s[db * kApplyTile + r] = __frcp_rn(p + kDenEps);
                 }
                 mbar_arrive(tab_empty0 + 8u * slot);
             }
