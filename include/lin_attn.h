@@ -191,14 +191,20 @@ int lin_attn_debug_kv(lin_attn_ctx *ctx, float *kv_out, struct CUstream_st *stre
 int lin_attn_device_status(lin_attn_ctx *ctx, struct CUstream_st *stream);
 
 /*
- * Work split of the KV reduction for this shape and tier.  Each head's 64-token tiles
- * are cut into k = min(152 / heads, tiles per head, 150) (at least 1) contiguous chunks of
- * equal size, at the same token boundaries for every head; `*chunks` = k * heads (one CTA
- * each), and each head's k partial D x D sums (`*max_segments` = k) are added in a fixed
- * pairwise order.  The split depends on (heads, n_tokens) only - never on the GPU or the
- * activation layout - which is what makes the summation order, and so the result,
- * reproducible (both tiers and both layouts use the same split).  Either out-pointer may
- * be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad arguments.
+ * Work split of the KV reduction for this shape and tier.  k = min(152 / heads, tiles per
+ * head, 150) (at least 1) chunks per head take each head's leading 64-token tiles, cut at
+ * the same tokens for every head.  On long sequences (at least 256 tiles per such chunk)
+ * with k * heads < 152, the 152 - k * heads spare chunks share the remaining tiles of all
+ * heads (taken head after head) in equal parts; the number of leading tiles is chosen so
+ * that the costliest chunk is as cheap as possible (a chunk that runs into another head
+ * counts 6 tiles more per head), and the spare chunks are used only where that beats the
+ * split without them.  `*chunks` = one CTA each (152 for the 720p layer at 20 or 32
+ * heads), and each head's partial D x D sums - one per chunk run that lies in the head: k,
+ * plus one or two from the shared tiles; the most any head has is `*max_segments` - are
+ * added in a fixed pairwise order.  The split depends on (heads, n_tokens) only - never on
+ * the GPU or the activation layout - which is what makes the summation order, and so the
+ * result, reproducible (both tiers and both layouts use the same split).  Either
+ * out-pointer may be NULL.  Returns LIN_ATTN_ERR_INVALID_ARG on bad arguments.
  */
 int lin_attn_kv_plan(int heads, int64_t n_tokens, int mode, int *chunks, int *max_segments);
 
@@ -243,7 +249,7 @@ int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *event
  *     + heads * 3 * ceil(head_dim / 64) * head_dim * 128   (the KV image)
  *     + 256                                 (status word)
  *     A shape that needs more than 48 MiB is rejected with LIN_ATTN_ERR_INVALID_ARG.  The
- *     720p/193-frame layer (20 x 180320 x 112, k = 7) needs ~9.3 MiB; at head_dim 128 and
+ *     720p/193-frame layer (20 x 180320 x 112, 9 slots) needs ~11.2 MiB; at head_dim 128 and
  *     1 slot per head (heads >= 153) the limit is 219 heads.
  *   - The first call on a device resolves the array's device address (cudaGetSymbolAddress,
  *     with that device current) and keeps it; a failed attempt is not kept, so the next

@@ -69,7 +69,7 @@ int main(void) {
     if (strstr(lin_attn_last_error(), "head_dim") == NULL) return 15;
     int chunks = 0, segs = 0;
     if (lin_attn_kv_plan(20, 180320, LIN_ATTN_MODE_HIGH, &chunks, &segs) != LIN_ATTN_OK) return 16;
-    if (chunks != 140 || segs != 7) return 17;
+    if (chunks != 152 || segs != 9) return 17;
     if (lin_attn_kv_plan(0, 10, LIN_ATTN_MODE_HIGH, &chunks, &segs) != LIN_ATTN_ERR_INVALID_ARG) return 18;
     if (lin_attn_destroy(NULL) != LIN_ATTN_OK) return 19;
     puts("ok");
@@ -137,22 +137,29 @@ def test_noalloc_entry_checks_arguments_before_any_cuda_call(la):
 
 def test_kv_plan_depends_on_shape_and_tier_only(la):
     # The plan fixes the summation order: a pure function of (H, N, tier) that keeps every
-    # head within the reduction's 160-partial budget.  Each head's 64-token tiles are cut
-    # into k = max(1, min(152 // H, tiles per head, 150)) chunks at the same token
-    # boundaries for every head: G = k H chunks, k partials per head.
+    # head within the reduction's 160-partial budget.  k = max(1, min(152 // H, tiles per
+    # head, 150)) chunks per head take each head's leading tiles, cut at the same tokens;
+    # on long sequences the spare CTAs (152 - k H) share the rest, so a head has k, k + 1
+    # or k + 2 partials.  (tests/test_work_split.py checks the partition tile by tile.)
     for H in (1, 2, 12, 20, 32, 64, 151, 152, 153, 4096):
         for N in (1, 63, 64, 65, 256, 1000, 32760, 180320, 262144):
             if H * N >= 2 ** 31:
                 continue
+            tiles = -(-N // 64)
             for mode in ("high", "lossless"):
                 G, segs = la.kv_plan(H, N, mode)
-                assert (G, segs) == la.kv_plan(H, N, mode)
-                k = max(1, min(152 // H, -(-N // 64), 150))
-                assert (G, segs) == (k * H, k)
+                assert (G, segs) == la.kv_plan(H, N, mode) == la.kv_plan(H, N, "lossless")
+                k = max(1, min(152 // H, tiles, 150))
+                if k * H >= 152 or k == tiles or G == k * H:  # no spare CTAs, or no tail worth it
+                    assert (G, segs) == (k * H, k)
+                else:
+                    assert k * H < G <= 152 and k < segs <= k + 2
                 assert 1 <= segs <= 160
-    assert la.kv_plan(20, 180320, "high") == (140, 7)
-    assert la.kv_plan(20, 180320, "lossless") == (140, 7)
-    assert la.kv_plan(32, 180320, "high") == (128, 4)
+    assert la.kv_plan(20, 180320, "high") == (152, 9)
+    assert la.kv_plan(20, 180320, "lossless") == (152, 9)
+    assert la.kv_plan(32, 180320, "high") == (152, 6)
+    assert la.kv_plan(152, 180320, "high") == (152, 1)
+    assert la.kv_plan(20, 32760, "high") == (140, 7)  # 480p: parts too short for a tail
     with pytest.raises(la.LinAttnError):
         la.kv_plan(0, 10, "high")
 

@@ -53,7 +53,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kApplyThreads, 1)
     apply_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                     const uint8_t* kv_image, const float* __restrict__ den, int heads, int n_tokens,
-                    int head_dim, int tiles_per_head, int token_major, int* status, uint64_t wait_ns) {
+                    int head_dim, const TileSplit sp, int token_major, int* status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -80,18 +80,18 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Head-major activations: contiguous ranges of the layer's (head, tile) sequence.
-    // Token-major: gridDim = k heads, CTA b takes part b % k of head b / k, every head cut
-    // at the same tiles, so the CTAs running together read and write the same token rows.
+    // Head-major activations: contiguous ranges of the layer's (head, tile) sequence (sp has
+    // no tail: tile t is tile t % T of head t / T).  Token-major: the CTAs are the chunks of
+    // the body + tail split sp (every head's body cut at the same tiles, so the CTAs running
+    // together read and write the same token rows; the spare CTAs share the tails).
     int t_begin, t_end;
     if (!token_major) {
-        const int total = heads * tiles_per_head;
+        const int total = heads * static_cast<int>(sp.tiles_per_head);
         t_begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
         t_end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
     } else {
-        const int k = gridDim.x / heads, hb = blockIdx.x / k, g = blockIdx.x % k;
-        t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k);
-        t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k);
+        t_begin = static_cast<int>(split_begin(sp, blockIdx.x));
+        t_end = static_cast<int>(split_begin(sp, blockIdx.x + 1));
     }
 
     if (threadIdx.x == 0) {
@@ -138,8 +138,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             int cur_h = -1, run = -1;
             bool b_pending = false;
             for (int t = t_begin; t < t_end; ++t, ++it) {
-                const int h = t / tiles_per_head;
-                const int n0 = (t % tiles_per_head) * kApplyTile;
+                int h, tile;
+                split_tile32(sp, t, h, tile);
+                const int n0 = tile * kApplyTile;
                 const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
                 if (!mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kQAtomBytes);
@@ -180,7 +181,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             for (int t = t_begin; t < t_end; ++t, ++it) {
-                const int h = t / tiles_per_head;
+                int h, tile;
+                split_tile32(sp, t, h, tile);
                 const uint32_t lt = static_cast<uint32_t>(t - t_begin);
                 if (h != cur_h) {
                     if (run >= 0) mma_commit(b_empty);  // old image free once its MMAs are done
@@ -230,8 +232,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         const int g_per = (groups + 1) / 2;
         const int g_lo = eh * g_per, g_hi = min(groups, g_lo + g_per);
         for (int t = t_begin; t < t_end; ++t) {
-            const int h = t / tiles_per_head;
-            const int n0 = (t % tiles_per_head) * kApplyTile;
+            int h, tile;
+            split_tile32(sp, t, h, tile);
+            const int n0 = tile * kApplyTile;
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
             const int row0 = n0 + 32 * q;
             const int row = row0 + lane;
@@ -302,15 +305,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
 
 template <int NBOX, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
-                      int heads, int n_tokens, int head_dim, bool token_major, int grid, int* status,
-                      uint64_t wait_ns, cudaStream_t stream) {
+                      int heads, int n_tokens, int head_dim, bool token_major, const TileSplit& sp, int grid,
+                      int* status, uint64_t wait_ns, cudaStream_t stream) {
     const uint32_t smem = apply_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
     return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
-                             img, den, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, wait_ns);
+                             img, den, heads, n_tokens, head_dim, sp, token_major ? 1 : 0, status, wait_ns);
 }
 
 }  // namespace
@@ -321,17 +323,20 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
     const int n = static_cast<int>(n_tokens);
     const int tph = (n + kApplyTile - 1) / kApplyTile;
     const int total = heads * tph;
-    if (grid > total) grid = total;
-    if (token_major) {  // a whole number of CTAs per head (see the kernel's schedule)
-        const int k = std::max(1, std::min(grid / heads, tph));
-        grid = k * heads;
+    TileSplit sp;
+    if (token_major) {  // the CTAs are the chunks of the split (see the kernel's schedule)
+        sp = tile_split(heads, tph, grid, kNoPerHeadCap, kApplyMinPart, kApplySwitchCost);
+        grid = sp.chunks;
+    } else {  // whole heads, no tail: only the tile -> (head, tile) map is used
+        sp = tile_split(heads, tph, heads, 1, 0, 0);
+        if (grid > total) grid = total;
     }
     const bool one = head_dim_atoms(head_dim) == 1;
-    if (one)
-        return out_bf16 ? launch_tc<1, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream)
-                        : launch_tc<1, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream);
-    return out_bf16 ? launch_tc<2, true>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream)
-                    : launch_tc<2, false>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, grid, status, wait_ns, stream);
+#define LA_APPLY(NB, BF) \
+    launch_tc<NB, BF>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, sp, grid, status, wait_ns, stream)
+    if (one) return out_bf16 ? LA_APPLY(1, true) : LA_APPLY(1, false);
+    return out_bf16 ? LA_APPLY(2, true) : LA_APPLY(2, false);
+#undef LA_APPLY
 }
 
 }  // namespace la

@@ -79,7 +79,7 @@ template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
     apply_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
                        const uint8_t* kv_image, int heads, int n_tokens, int head_dim,
-                       int tiles_per_head, int token_major, int* status, uint64_t wait_ns,
+                       const TileSplit sp, int token_major, int* status, uint64_t wait_ns,
                        const ProducerArgs pa) {
     constexpr int kStages = fused_stages(NBOX);
     extern __shared__ uint8_t smem_raw[];
@@ -111,15 +111,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // gridDim = k heads: CTA b takes part b % k of head b / k, every head cut at the same
-    // tiles, so the CTAs running together work on the same token rows.  They then read each
-    // rotation-table row (the same for every head) from DRAM once, and token-major
-    // activations on whole DRAM rows.  (Contiguous ranges of the (head, tile) sequence keep
-    // all 152 SMs busy, but the CTAs then walk the whole token range at once and the 80 MB of
-    // tables at 720p were read from DRAM about five times: 0.8 % slower per call.)
-    const int k_per_head = gridDim.x / heads, hb = blockIdx.x / k_per_head, g = blockIdx.x % k_per_head;
-    const int t_begin = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * g / k_per_head);
-    const int t_end = hb * tiles_per_head + static_cast<int>(static_cast<int64_t>(tiles_per_head) * (g + 1) / k_per_head);
+    // The CTAs are the chunks of the body + tail split sp: k CTAs per head take the first
+    // B tiles of their head, cut at the same tiles for every head, so the CTAs running
+    // together work on the same token rows.  They then read each rotation-table row (the
+    // same for every head) from DRAM once, and token-major activations on whole DRAM rows.
+    // The 152 - k H spare CTAs share the remaining tiles of all heads (a few MB of tables,
+    // which stay in L2).  (Contiguous ranges of the (head, tile) sequence keep all SMs busy
+    // too, but the CTAs then walk the whole token range at once and the 80 MB of tables at
+    // 720p were read from DRAM about five times: 0.8 % slower per call.)
+    const int t_begin = static_cast<int>(split_begin(sp, blockIdx.x));
+    const int t_end = static_cast<int>(split_begin(sp, blockIdx.x + 1));
     const uint32_t half_d = static_cast<uint32_t>(head_dim / 2);  // image columns per term
 
     if (threadIdx.x == 0) {
@@ -172,8 +173,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
             bool ok = true;
             for (int t = t_begin; t < t_end && ok; ++t) {
                 const uint32_t it = static_cast<uint32_t>(t - t_begin);
-                const int h = t / tiles_per_head;
-                const int n0 = (t % tiles_per_head) * kApplyTile;
+                int h, tile;
+                split_tile32(sp, t, h, tile);
+                const int n0 = tile * kApplyTile;
                 const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
                 if (!(ok = mbar_wait(q_empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns))) break;
                 mbar_arrive_expect_tx(q_full0 + 8u * st, NBOX * kFQAtom);
@@ -219,7 +221,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
             uint32_t it = 0;
             int cur_h = -1, run = -1;
             for (int t = t_begin; t < t_end; ++t, ++it) {
-                const int h = t / tiles_per_head;
+                int h, tile;
+                split_tile32(sp, t, h, tile);
                 const uint32_t lt = static_cast<uint32_t>(t - t_begin);
                 if (h != cur_h) {
                     if (run >= 0) mma_commit(b_empty);  // the old image is free once its MMAs are done
@@ -266,8 +269,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         int cur_h = -1;
         uint32_t it = 0;
         for (int t = t_begin; t < t_end; ++t, ++it) {
-            const int h = t / tiles_per_head;
-            const int n0 = (t % tiles_per_head) * kApplyTile;
+            int h, tile;
+            split_tile32(sp, t, h, tile);
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
             if (h != cur_h) {
                 if (cur_h < 0) grid_dependency_wait();  // the column sums come from the reduction
@@ -363,8 +366,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         int cur_h = -1, run = -1;
         bool ok = true;
         for (int t = t_begin; t < t_end && ok; ++t) {
-            const int h = t / tiles_per_head;
-            const int n0 = (t % tiles_per_head) * kApplyTile;
+            int h, tile;
+            split_tile32(sp, t, h, tile);
+            const int n0 = tile * kApplyTile;
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
             if (h != cur_h) {
                 // The head's image into TMEM: feature j's row of each term (input features i as
@@ -462,15 +466,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
 template <int NBOX, bool BF16>
 cudaError_t launch(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, int heads, int n_tokens,
-                   int head_dim, bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream,
-                   const ProducerArgs& pa) {
+                   int head_dim, bool token_major, const TileSplit& sp, int* status, uint64_t wait_ns,
+                   cudaStream_t stream, const ProducerArgs& pa) {
     const uint32_t smem = fused_smem_bytes(head_dim);
     cudaError_t e = cudaFuncSetAttribute(apply_fused_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int tph = (n_tokens + kApplyTile - 1) / kApplyTile;
-    return launch_overlapped(apply_fused_kernel<NBOX, BF16>, dim3(grid), dim3(kFThreads), smem, stream, tm_q, tm_out,
-                             img, heads, n_tokens, head_dim, tph, token_major ? 1 : 0, status, wait_ns, pa);
+    return launch_overlapped(apply_fused_kernel<NBOX, BF16>, dim3(sp.chunks), dim3(kFThreads), smem, stream, tm_q,
+                             tm_out, img, heads, n_tokens, head_dim, sp, token_major ? 1 : 0, status, wait_ns, pa);
 }
 
 }  // namespace
@@ -480,17 +483,12 @@ cudaError_t launch_apply_fused_tc(const CUtensorMap& tm_q, const CUtensorMap& tm
                                   int* status, uint64_t wait_ns, cudaStream_t stream, const ProducerArgs& producer) {
     const int n = static_cast<int>(n_tokens);
     const int tph = (n + kApplyTile - 1) / kApplyTile;
-    const int total = heads * tph;
-    if (grid > total) grid = total;
-    {  // a whole number of CTAs per head (see the kernel's schedule)
-        const int k = grid / heads < 1 ? 1 : (grid / heads < tph ? grid / heads : tph);
-        grid = k * heads;
-    }
-    if (head_dim_atoms(head_dim) == 1)
-        return out_bf16 ? launch<1, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer)
-                        : launch<1, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer);
-    return out_bf16 ? launch<2, true>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer)
-                    : launch<2, false>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, grid, status, wait_ns, stream, producer);
+    const TileSplit sp = tile_split(heads, tph, grid, kNoPerHeadCap, kApplyMinPart, kApplySwitchCost);  // a CTA per chunk
+#define LA_FUSED(NB, BF) \
+    launch<NB, BF>(tm_q, tm_out_t, kv_image, heads, n, head_dim, token_major, sp, status, wait_ns, stream, producer)
+    if (head_dim_atoms(head_dim) == 1) return out_bf16 ? LA_FUSED(1, true) : LA_FUSED(1, false);
+    return out_bf16 ? LA_FUSED(2, true) : LA_FUSED(2, false);
+#undef LA_FUSED
 }
 
 }  // namespace la

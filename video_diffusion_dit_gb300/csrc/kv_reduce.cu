@@ -58,15 +58,22 @@ struct KvLayout {
     static constexpr uint32_t sum_col = 256;
 };
 
-// Tiles [t_s, t_e) of the CTA's chunk, clipped to the launch's head range.
+// Virtual tiles [t_s, t_e) of the CTA's chunk (see TileSplit), clipped to the launch's heads.
 struct ChunkTiles {
     int64_t c, t_s, t_e;
 };
 __device__ __forceinline__ ChunkTiles chunk_tiles(const KvPlan& plan, const KvLaunch& work) {
     ChunkTiles r;
-    r.c = work.c_lo + blockIdx.x;
-    r.t_s = max(chunk_begin(plan, r.c), work.t_lo);
-    r.t_e = min(chunk_begin(plan, r.c + 1), work.t_hi);
+    const int b = static_cast<int>(blockIdx.x);
+    if (b < work.n_body) {
+        r.c = work.c_body + b;
+        r.t_s = split_begin(plan, r.c);
+        r.t_e = split_begin(plan, r.c + 1);
+    } else {
+        r.c = work.c_tail + (b - work.n_body);
+        r.t_s = max(split_begin(plan, r.c), work.tail_lo);
+        r.t_e = min(split_begin(plan, r.c + 1), work.tail_hi);
+    }
     return r;
 }
 
@@ -95,7 +102,6 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const ChunkTiles ct = chunk_tiles(plan, work);
-    const int64_t tph = plan.tiles_per_head;
     // The MMA consumes a stage once it is loaded (full) or, on the fused path, transformed.
     const uint32_t mma_ready0 = FUSED ? ready0 : full0;
 
@@ -152,8 +158,9 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             const uint64_t tab_pol = policy_evict_last();
             uint32_t it = 0;
             for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
-                const int h = static_cast<int>(t / tph);
-                const int y = static_cast<int>((t % tph) * kKvTile);
+                const HeadTile ht = split_tile(plan, t);
+                const int h = ht.h;
+                const int y = static_cast<int>(ht.tile * kKvTile);
                 const int c1 = token_major ? h - work.h0 : y, c2 = token_major ? y : h - work.h0;
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
                 if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             uint32_t it = 0, sub = 0;
             bool ok = true;
             for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
-                const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+                const int64_t seg_end = min(ct.t_e, split_run_end(plan, t));
                 for (int64_t k0 = t; ok && k0 < seg_end; k0 += PROMOTE, ++sub) {
                     const int64_t k1 = min(k0 + PROMOTE, seg_end);
                     const uint32_t buf = sub & 1u;
@@ -235,8 +242,8 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
-            const int h = static_cast<int>(t / tph);
-            const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+            const int h = split_tile(plan, t).h;
+            const int64_t seg_end = min(ct.t_e, split_run_end(plan, t));
             // Column sums of relu(K): each tile's 8 rows in plain binary32 pairs, folded into a
             // compensated binary32 running sum (sum + running error term) once per tile, in a
             // fixed order: FP64-class accuracy at FP32 rate.  Pair e holds columns
@@ -314,8 +321,8 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         uint32_t sub = 0;
         bool ok = true;
         for (int64_t t = ct.t_s; ok && t < ct.t_e;) {
-            const int h = static_cast<int>(t / tph);
-            const int64_t seg_end = min(ct.t_e, (t / tph + 1) * tph);
+            const int h = split_tile(plan, t).h;
+            const int64_t seg_end = min(ct.t_e, split_run_end(plan, t));
             float acc[FUSED ? 1 : 64 * NBOX];
             if constexpr (!FUSED) {
 #pragma unroll
@@ -625,7 +632,7 @@ cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_imag
     dim3 grid(head_dim / 8, hc);
     const double* kp = producer ? producer->ksum_partial : nullptr;
     float* ks = producer ? producer->ksum : nullptr;
-    if (plan.per_head <= kSmallSegs)
+    if (plan.seg_stride <= kSmallSegs)
         return launch_overlapped(kv_finalize_kernel<true>, grid, dim3(256), 0, stream, partial, kv, kv_image, h0,
                                  head_dim, plan, kp, ks);
     return launch_overlapped(kv_finalize_kernel<false>, grid, dim3(256), 0, stream, partial, kv, kv_image, h0, head_dim,

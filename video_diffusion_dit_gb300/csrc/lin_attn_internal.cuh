@@ -15,78 +15,210 @@ namespace la {
 constexpr int kKvTile = 64;
 // Token tile of the tensor-core apply kernel (MMA M).
 constexpr int kApplyTile = 128;
-// Work chunks of the KV reduction.  Each head's 64-token tiles are cut into k contiguous
-// chunks of equal size (+-1 tile), at the same token boundaries for every head:
-// k = min(floor(152 / H), tiles per head, 150), at least 1, and G = k H chunks in head
-// order (chunk c is part c % k of head c / k).  Each chunk is summed by one CTA and leaves
-// one partial KV.  With every head cut at the same tokens, the CTAs that run at the same
-// time walk the same token rows of all heads, which keeps reads of token-major [N, H, D]
-// activations on whole DRAM rows.  k and G are constants of the shape (152 = one chunk per
-// SM of a 152-SM part), never read from the device, so the summation order is fixed by the
-// shape.
-constexpr int kChunks = 152;
-constexpr int kChunksPerHeadCap = 150;  // k <= 150 keeps a head under kMaxSegments partials
-constexpr int kMaxSegments = 160;       // partials per head the reduction can add
-
-struct KvPlan {
-    int64_t tiles_per_head;  // ceil(N / kKvTile)
-    int64_t total_tiles;     // H * tiles_per_head
-    int chunks;              // G = k H
-    int per_head;            // k: chunks (and partials) per head
-    int seg_stride;          // partial slots per head (= k)
+// ---------------------------------------------------------------- work split
+// H heads x T tiles shared out over G CTAs.  k = min(floor(G / H), T, cap) (at least 1)
+// CTAs per head take the head's first B tiles (the body), cut into k equal parts (+-1
+// tile) at the same tiles for every head, so the CTAs running at the same time walk the
+// same token rows of all heads: reads of token-major [N, H, D] activations stay on whole
+// DRAM rows, and rotation-table rows fetched for one head are served to the others from
+// L2.  The E = G - k H CTAs left over (if any) may share the rest (the tail: tiles [B, T)
+// of every head, concatenated head after head) in equal parts.  A tail part that runs
+// into another head pays for the switch (a new head's operands, a partial written), so B
+// is chosen to minimise the longest part counting `switch_cost` tiles per extra head, and
+// the tail is used only where parts are long (T / k >= min_part) and it makes the longest
+// part shorter.  Chunk c < k H is part c % k of head c / k's body; chunk k H + e is part e
+// of the tail.
+//
+// Chunks are ranges of a virtual order of the tiles: every head's body (head-major), then
+// every head's tail.  A chunk's run of tiles of one head is a segment; a body chunk is one
+// segment, a tail chunk one per head it touches.
+struct TileSplit {
+    int heads;
+    int per_head;            // k: body chunks per head
+    int tail_chunks;         // E
+    int chunks;              // k H + E
+    int64_t tiles_per_head;  // T
+    int64_t body;            // B (T when there is no tail)
 };
 
-__host__ __device__ inline int kv_chunks_per_head(int heads, int64_t tiles_per_head) {
-    int64_t k = kChunks / heads;
+// Longest tail part, counting `switch_cost` per head beyond its first, for body length b
+// and e parts (e >= 1, b < T).
+__host__ __device__ inline int64_t tail_part_cost(int heads, int64_t tiles_per_head, int64_t b, int64_t e,
+                                                  int64_t switch_cost) {
+    const int64_t tl = tiles_per_head - b, all = heads * tl;
+    int64_t most = 0;
+    for (int64_t j = 0; j < e; ++j) {
+        const int64_t u0 = j * all / e, u1 = (j + 1) * all / e;
+        const int64_t cost = (u1 - u0) + switch_cost * ((u1 - 1) / tl - u0 / tl);
+        most = cost > most ? cost : most;
+    }
+    return most;
+}
+
+__host__ __device__ inline TileSplit tile_split(int heads, int64_t tiles_per_head, int ctas, int per_head_cap,
+                                                int64_t min_part, int64_t switch_cost) {
+    TileSplit s;
+    s.heads = heads;
+    s.tiles_per_head = tiles_per_head;
+    int64_t k = ctas / heads;
     if (k > tiles_per_head) k = tiles_per_head;
-    if (k > kChunksPerHeadCap) k = kChunksPerHeadCap;
-    return k < 1 ? 1 : static_cast<int>(k);
+    if (k > per_head_cap) k = per_head_cap;
+    if (k < 1) k = 1;
+    s.per_head = static_cast<int>(k);
+    s.body = tiles_per_head;
+    s.tail_chunks = 0;
+    const int64_t spare = static_cast<int64_t>(ctas) - k * heads;
+    const int64_t no_tail = (tiles_per_head + k - 1) / k;
+    if (spare > 0 && k < tiles_per_head && tiles_per_head / k >= min_part) {
+        // Equal costs near B = k (H T + switch_cost * ceil(H / E) * E) / G; the candidates
+        // around it are costed exactly and the first cheapest is taken.
+        const int64_t extra = switch_cost * ((heads + spare - 1) / spare) * spare;
+        const int64_t b0 = k * (heads * tiles_per_head + extra) / ctas;
+        int64_t best = -1, best_cost = no_tail;
+        for (int64_t b = b0 - 2; b <= b0 + 2; ++b) {
+            if (b < k || b >= tiles_per_head) continue;
+            const int64_t tail = heads * (tiles_per_head - b), e = spare < tail ? spare : tail;
+            const int64_t body_cost = (b + k - 1) / k;
+            const int64_t tail_cost = tail_part_cost(heads, tiles_per_head, b, e, switch_cost);
+            const int64_t cost = body_cost > tail_cost ? body_cost : tail_cost;
+            if (cost < best_cost) {
+                best = b;
+                best_cost = cost;
+            }
+        }
+        if (best >= 0) {
+            const int64_t tail = heads * (tiles_per_head - best);
+            s.body = best;
+            s.tail_chunks = static_cast<int>(spare < tail ? spare : tail);
+        }
+    }
+    s.chunks = s.per_head * heads + s.tail_chunks;
+    return s;
+}
+// Tiles in the tail of one head (T - B) and in all tails.
+__host__ __device__ inline int64_t split_tail_len(const TileSplit& s) { return s.tiles_per_head - s.body; }
+// First virtual tile of chunk c, for c in [0, chunks]; chunk c covers [begin(c), begin(c + 1)).
+__host__ __device__ inline int64_t split_begin(const TileSplit& s, int64_t c) {
+    const int64_t kh = static_cast<int64_t>(s.per_head) * s.heads;
+    if (c < kh) return (c / s.per_head) * s.body + (c % s.per_head) * s.body / s.per_head;
+    const int64_t all_tails = s.heads * split_tail_len(s);
+    return s.heads * s.body + (s.tail_chunks ? (c - kh) * all_tails / s.tail_chunks : 0);
+}
+// Head and tile (within the head) of virtual tile v.
+struct HeadTile {
+    int h;
+    int64_t tile;
+};
+__host__ __device__ inline HeadTile split_tile(const TileSplit& s, int64_t v) {
+    const int64_t hb = s.heads * s.body;
+    if (v < hb) return HeadTile{static_cast<int>(v / s.body), v % s.body};
+    const int64_t u = v - hb, tl = split_tail_len(s);
+    return HeadTile{static_cast<int>(u / tl), s.body + u % tl};
+}
+// End of the run of virtual tiles that holds v and stays in one head's body or tail.
+__host__ __device__ inline int64_t split_run_end(const TileSplit& s, int64_t v) {
+    const int64_t hb = s.heads * s.body;
+    if (v < hb) return (v / s.body + 1) * s.body;
+    const int64_t tl = split_tail_len(s);
+    return hb + ((v - hb) / tl + 1) * tl;
+}
+// Tail part that holds unit u of the concatenated tails (needs tail_chunks > 0).
+__host__ __device__ inline int64_t split_tail_part(const TileSplit& s, int64_t u) {
+    return ((u + 1) * s.tail_chunks - 1) / (s.heads * split_tail_len(s));
+}
+
+// split_tile in 32-bit arithmetic, for splits of fewer than 2^31 tiles.
+__host__ __device__ inline void split_tile32(const TileSplit& s, int v, int& h, int& tile) {
+    const int b = static_cast<int>(s.body), hb = s.heads * b;
+    if (v < hb) {
+        h = v / b;
+        tile = v - h * b;
+    } else {
+        const int tl = static_cast<int>(s.tiles_per_head) - b, u = v - hb;
+        h = u / tl;
+        tile = b + (u - h * tl);
+    }
+}
+// The apply kernels' schedules: no cap on the CTAs per head; a tail only where a CTA has
+// at least 96 tiles (12288 tokens) of a head; a head switch in a tail part costs about 4
+// tiles (its KV image is loaded and the pipeline refills).
+constexpr int kNoPerHeadCap = 1 << 30;
+constexpr int64_t kApplyMinPart = 96;
+constexpr int64_t kApplySwitchCost = 4;
+
+// Work chunks of the KV reduction: the split above of the layer's 64-token tiles over
+// G = 152 chunks (one per SM of a 152-SM part) with k <= 150, a tail only where a chunk
+// has at least 256 tiles (16384 tokens) of a head, and a head switch counted as 6 tiles
+// (a partial written, the next head's first tiles refill the pipeline).  Each segment is summed by
+// one CTA and leaves one partial KV: head h has k body partials (slots 0..k-1) and one or
+// two tail partials (slots k, k+1).  The split is a function of (H, N) only, never read
+// from the device, so the summation order is fixed by the shape.
+constexpr int kChunks = 152;
+constexpr int kChunksPerHeadCap = 150;  // k + 2 <= 152 keeps a head under kMaxSegments partials
+constexpr int64_t kKvMinPart = 256;
+constexpr int64_t kKvSwitchCost = 6;
+constexpr int kMaxSegments = 160;       // partials per head the reduction can add
+
+struct KvPlan : TileSplit {
+    int seg_stride;  // partial slots per head: the most segments any head has
+};
+
+// Partial slot of (head h, chunk c) and the number of partials of head h.
+__host__ __device__ inline int segment_of(const KvPlan& p, int h, int64_t c) {
+    const int64_t kh = static_cast<int64_t>(p.per_head) * p.heads;
+    if (c < kh) return static_cast<int>(c % p.per_head);
+    const int64_t first = split_tail_part(p, static_cast<int64_t>(h) * split_tail_len(p));
+    return p.per_head + static_cast<int>(c - kh - first);
+}
+__host__ __device__ inline int segments_of_head(const KvPlan& p, int h) {
+    if (p.tail_chunks == 0) return p.per_head;
+    const int64_t tl = split_tail_len(p);
+    return p.per_head + static_cast<int>(split_tail_part(p, (h + 1) * tl - 1) - split_tail_part(p, h * tl) + 1);
 }
 __host__ __device__ inline KvPlan kv_plan(int heads, int64_t n_tokens) {
     KvPlan p;
-    p.tiles_per_head = (n_tokens + kKvTile - 1) / kKvTile;
-    p.total_tiles = p.tiles_per_head * heads;
-    p.per_head = kv_chunks_per_head(heads, p.tiles_per_head);
-    p.chunks = p.per_head * heads;
+    static_cast<TileSplit&>(p) = tile_split(heads, (n_tokens + kKvTile - 1) / kKvTile, kChunks, kChunksPerHeadCap,
+                                            kKvMinPart, kKvSwitchCost);
     p.seg_stride = p.per_head;
+    for (int h = 0; p.tail_chunks > 0 && h < heads; ++h) {
+        const int n = segments_of_head(p, h);
+        if (n > p.seg_stride) p.seg_stride = n;
+    }
     return p;
 }
-// First tile of chunk c (chunk c covers [chunk_begin(c), chunk_begin(c + 1))).
-__host__ __device__ inline int64_t chunk_begin(const KvPlan& p, int64_t c) {
-    const int64_t h = c / p.per_head, g = c % p.per_head;
-    return h * p.tiles_per_head + g * p.tiles_per_head / p.per_head;
-}
-// The chunk that holds tile t.
-__host__ __device__ inline int64_t chunk_of_tile(const KvPlan& p, int64_t t) {
-    const int64_t h = t / p.tiles_per_head, lt = t % p.tiles_per_head;
-    return h * p.per_head + ((lt + 1) * p.per_head - 1) / p.tiles_per_head;
-}
-// Partial slot of (head h, chunk c) and the number of partials of head h.
-__host__ __device__ inline int segment_of(const KvPlan& p, int h, int64_t c) {
-    return static_cast<int>(c - static_cast<int64_t>(h) * p.per_head);
-}
-__host__ __device__ inline int segments_of_head(const KvPlan& p, int) { return p.per_head; }
-// Largest seg_stride any n_tokens can produce for `heads` (scratch sizing).
+// Largest seg_stride any n_tokens can produce for `heads` (scratch sizing): k is at most
+// min(152 / H, 150), and a head's tail is never split more than twice (a tail part holds
+// at least one head's whole tail, since E < H whenever k = floor(152 / H)).
 __host__ __device__ inline int kv_seg_stride_bound(int heads) {
-    return kv_chunks_per_head(heads, static_cast<int64_t>(kChunksPerHeadCap));
+    const int k = tile_split(heads, kChunksPerHeadCap, kChunks, kChunksPerHeadCap, 0, 0).per_head;
+    return k + (kChunks - k * heads > 0 ? 2 : 0);
 }
 
 // Work of one launch of the KV reduction: heads [h0, h0 + hc) of the layer (the K/V
-// pointers and tensor maps start at head h0), i.e. tiles [t_lo, t_hi) of chunks
-// [c_lo, c_hi].
+// pointers and tensor maps start at head h0): their body chunks, then the tail chunks that
+// touch them, each clipped to those heads.
 struct KvLaunch {
     int h0;
-    int64_t t_lo, t_hi;
-    int64_t c_lo;
-    int n_chunks;
+    int n_body;                   // CTAs [0, n_body): body chunks c_body ...
+    int n_chunks;                 // CTAs [n_body, n_chunks): tail chunks c_tail ...
+    int64_t c_body, c_tail;
+    int64_t tail_lo, tail_hi;     // virtual tiles of these heads' tails
 };
 __host__ __device__ inline KvLaunch kv_launch(const KvPlan& p, int h0, int hc) {
     KvLaunch l;
     l.h0 = h0;
-    l.t_lo = h0 * p.tiles_per_head;
-    l.t_hi = (h0 + hc) * p.tiles_per_head;
-    l.c_lo = chunk_of_tile(p, l.t_lo);
-    l.n_chunks = static_cast<int>(chunk_of_tile(p, l.t_hi - 1) - l.c_lo + 1);
+    l.c_body = static_cast<int64_t>(h0) * p.per_head;
+    l.n_body = hc * p.per_head;
+    l.n_chunks = l.n_body;
+    l.c_tail = l.tail_lo = l.tail_hi = 0;
+    if (p.tail_chunks > 0) {
+        const int64_t tl = split_tail_len(p), hb = p.heads * p.body;
+        const int64_t e_lo = split_tail_part(p, h0 * tl), e_hi = split_tail_part(p, (h0 + hc) * tl - 1);
+        l.c_tail = static_cast<int64_t>(p.per_head) * p.heads + e_lo;
+        l.n_chunks += static_cast<int>(e_hi - e_lo + 1);
+        l.tail_lo = hb + h0 * tl;
+        l.tail_hi = hb + (h0 + hc) * tl;
+    }
     return l;
 }
 
