@@ -294,10 +294,15 @@ __device__ __forceinline__ void rope_chunk(uint4& w, const float4 c4, const floa
     float x0[4], x1[4];
     const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
     const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+    const __nv_bfloat162 zero2 = __float2bfloat162_rn(0.f);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        x0[j] = fmaxf(__uint_as_float(in[j] << 16), 0.f);
-        x1[j] = fmaxf(__uint_as_float(in[j] & 0xFFFF0000u), 0.f);
+        // ReLU on the BF16 pair (one paired max; the same values as in binary32, a -0
+        // input may come out as either zero), then each half widened exactly.
+        const __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&in[j]), zero2);
+        const uint32_t rb = *reinterpret_cast<const uint32_t*>(&r);
+        x0[j] = __uint_as_float(rb << 16);
+        x1[j] = __uint_as_float(rb & 0xFFFF0000u);
         const float y0 = __fsub_rn(__fmul_rn(x0[j], cs[j]), __fmul_rn(x1[j], sn[j]));
         const float y1 = __fadd_rn(__fmul_rn(x0[j], sn[j]), __fmul_rn(x1[j], cs[j]));
         const __nv_bfloat162 y = __floats2bfloat162_rn(y0, y1);
