@@ -247,7 +247,7 @@ int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *event
  *       heads * k * head_dim^2 * 4          (FP32 partial sums)
  *     + heads * head_dim^2 * 4              (reduced KV)
  *     + heads * 3 * ceil(head_dim / 64) * head_dim * 128   (the KV image)
- *     + 256                                 (status word)
+ *     + 256                                 (status word, at the start of the array)
  *     A shape that needs more than 48 MiB is rejected with LIN_ATTN_ERR_INVALID_ARG.  The
  *     720p/193-frame layer (20 x 180320 x 112, 9 slots) needs ~11.2 MiB; at head_dim 128 and
  *     1 slot per head (heads >= 153) the limit is 219 heads.
@@ -258,12 +258,23 @@ int lin_attn_set_stage_events(lin_attn_ctx *ctx, struct CUevent_st *const *event
  *     clears what has to start at zero.  Calls that overlap on the GPU (from several
  *     streams or host threads) race on the array and corrupt each other's results, so
  *     serialise them.
- *   - A kernel that gives up waiting on one of its barriers is not reported by this
- *     entry point (there is no context to hold the status word).
+ *   - A kernel that gives up waiting on one of its barriers (its call's output is then
+ *     incomplete) is not reported by the call itself, which returns before the kernels
+ *     run: it is recorded in the array's status word, which lin_attn_noalloc_status reads.
  */
 int lin_attn_forward_noalloc(const void *q_rot, const void *k_rot, const void *v,
                              const float *normalizer, void *out, int out_dtype, int heads,
                              int64_t n_tokens, int head_dim, int mode, struct CUstream_st *stream);
+
+/*
+ * Status of the lin_attn_forward_noalloc calls on the calling thread's current device:
+ * waits for `stream` (the stream those calls were made on), then returns
+ * LIN_ATTN_ERR_TIMEOUT if a kernel of any of them since the previous query gave up
+ * waiting on one of its barriers, else LIN_ATTN_OK, and clears the record.  Makes no
+ * allocating call.  LIN_ATTN_ERR_CUDA / LIN_ATTN_ERR_UNSUPPORTED if the device cannot be
+ * queried.
+ */
+int lin_attn_noalloc_status(struct CUstream_st *stream);
 
 /* Static description of a status code. */
 const char *lin_attn_error_string(int status);

@@ -59,8 +59,8 @@ def context_call(la, g, mode, dt, dev):
 
 
 def scratch_bytes(la, H, N, D):
-    """Scratch the call needs: k partial slots per head of FP32 D x D sums, the reduced KV,
-    the three-term KV image and a status word, each rounded up to 256 bytes."""
+    """Scratch the call needs: a status word, k partial slots per head of FP32 D x D sums,
+    the reduced KV and the three-term KV image, each rounded up to 256 bytes."""
     _, k = la.kv_plan(H, N)
     up = lambda x: (x + 255) // 256 * 256
     return up(4 * D * D * H * k) + up(4 * D * D * H) + up(H * 3 * -(-D // 64) * D * 128) + 256
@@ -76,6 +76,7 @@ def test_two_calls_in_a_row_match_the_context_path(la, dev, mode, dt):
         torch.cuda.synchronize()
         want = context_call(la, g, mode, dt, dev)
         assert torch.equal(got, want), f"{mode} {dt} {tuple(g['q_rot'].shape)}: not bitwise the context call"
+        assert la.noalloc_status(dev) == la.OK  # no kernel of the call gave up waiting
         qb, kb, vb, den = oracle.torch_inputs_to_numpy(g)
         ref = oracle.forward(qb, kb, vb, den)
         err = rel_l2(got.double().cpu().numpy()[0], ref)

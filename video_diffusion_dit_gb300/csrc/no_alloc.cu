@@ -17,7 +17,9 @@
 // therefore come before any stream capture.  All
 // calls share the array and it keeps the previous call's contents: the parts that must
 // start at zero are cleared by every call, and calls whose execution overlaps on the GPU
-// (two streams, or two host threads) race on it and give wrong results.
+// (two streams, or two host threads) race on it and give wrong results.  Its first 256
+// bytes hold the status word, where a kernel that gave up waiting records the timeout;
+// lin_attn_noalloc_status reads and clears it.
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
@@ -31,6 +33,7 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;  // 48 MiB
 constexpr int kMaxDevices = 64;
+constexpr size_t kStatusBytes = 256;  // the status word's slot at the start of the scratch
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -87,6 +90,36 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(LIN_ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// The calling thread's current device's set-up, resolved on first use (see DeviceSetup).
+int device_setup(DeviceSetup* out) {
+    int device = -1;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device < 0 || device >= kMaxDevices) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device index %d too large", device);
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    DeviceSetup& slot = g_setup[device];
+    if (!slot.resolved) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is not sm_103", device);
+        unsigned char* addr = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&addr), g_noalloc_scratch);
+        if (e != cudaSuccess || !addr) {
+            cudaGetLastError();  // not sticky; leave the set-up open for the next call
+            return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        }
+        slot.scratch = addr;
+        slot.n_sms = sms;
+        slot.supported = true;
+        slot.resolved = true;
+    }
+    *out = slot;
+    return LIN_ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, const void* v,
@@ -106,7 +139,8 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
         if (reinterpret_cast<uintptr_t>(p) & 15u)
             return fail(LIN_ATTN_ERR_MISALIGNED, "every tensor pointer must be 16-byte aligned");
 
-    // Scratch carve-up: partials | KV | KV image | status word, each 256-byte aligned.
+    // Scratch carve-up: status word | partials | KV | KV image, each 256-byte aligned.  The
+    // status word sits at a fixed place so that lin_attn_noalloc_status can find it.
     const la::KvPlan plan = la::kv_plan(heads, n_tokens);
     const la::KvLaunch work = la::kv_launch(plan, 0, heads);
     const size_t dd = static_cast<size_t>(head_dim) * head_dim;
@@ -114,52 +148,27 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
     const size_t partial_bytes = up(sizeof(float) * dd * heads * plan.seg_stride);
     const size_t kv_bytes = up(sizeof(float) * dd * heads);
     const size_t image_bytes = static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads;
-    const size_t need = partial_bytes + kv_bytes + up(image_bytes) + 256;
+    const size_t need = kStatusBytes + partial_bytes + kv_bytes + up(image_bytes);
     if (need > kNoAllocScratchBytes)
         return fail(LIN_ATTN_ERR_INVALID_ARG,
                     "this shape needs %zu bytes of scratch, more than the %zu built into the library for "
                     "lin_attn_forward_noalloc; use a context (lin_attn_create) instead",
                     need, kNoAllocScratchBytes);
 
-    int device = -1;
-    cudaError_t e = cudaGetDevice(&device);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (device < 0 || device >= kMaxDevices) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device index %d too large", device);
     DeviceSetup su;
-    {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        DeviceSetup& slot = g_setup[device];
-        if (!slot.resolved) {
-            int major = 0, minor = 0, sms = 0;
-            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device)) != cudaSuccess ||
-                (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device)) != cudaSuccess ||
-                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
-                return cuda_fail(e, "cudaDeviceGetAttribute");
-            if (major != 10 || minor != 3) return fail(LIN_ATTN_ERR_UNSUPPORTED, "device %d is not sm_103", device);
-            unsigned char* addr = nullptr;
-            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&addr), g_noalloc_scratch);
-            if (e != cudaSuccess || !addr) {
-                cudaGetLastError();  // not sticky; leave the set-up open for the next call
-                return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-            }
-            slot.scratch = addr;
-            slot.n_sms = sms;
-            slot.supported = true;
-            slot.resolved = true;
-        }
-        su = slot;
-    }
+    if (const int rc = device_setup(&su)) return rc;
+    cudaError_t e;
 
-    float* partial = reinterpret_cast<float*>(su.scratch);
-    float* kv = reinterpret_cast<float*>(su.scratch + partial_bytes);
-    uint8_t* image = su.scratch + partial_bytes + kv_bytes;
-    int* status = reinterpret_cast<int*>(su.scratch + partial_bytes + kv_bytes + up(image_bytes));
+    int* status = reinterpret_cast<int*>(su.scratch);
+    float* partial = reinterpret_cast<float*>(su.scratch + kStatusBytes);
+    float* kv = reinterpret_cast<float*>(su.scratch + kStatusBytes + partial_bytes);
+    uint8_t* image = su.scratch + kStatusBytes + partial_bytes + kv_bytes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
 
-    // Must start at zero: the status word, and the KV image (its padding columns are read
-    // by the MMA and a previous call with another head dim may have left data there).
-    if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    // Must start at zero: the KV image (its padding columns are read by the MMA and a
+    // previous call with another head dim may have left data there).  The status word is
+    // not cleared here: it collects timeouts until lin_attn_noalloc_status reads it.
     if ((e = cudaMemsetAsync(image, 0, image_bytes, s)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
 
     CUtensorMap tk, tv;
@@ -180,5 +189,23 @@ extern "C" int lin_attn_forward_noalloc(const void* q_rot, const void* k_rot, co
     e = la::launch_apply_tc(tq, to, image, normalizer, heads, n_tokens, head_dim, bf16_out, false, su.n_sms, status,
                             la::kWaitLimitNs, s);
     if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    return la::record_error(LIN_ATTN_OK, "");
+}
+
+extern "C" int lin_attn_noalloc_status(struct CUstream_st* stream) {
+    DeviceSetup su;
+    if (const int rc = device_setup(&su)) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int* status = reinterpret_cast<int*>(su.scratch);
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the no-alloc status word");
+    if (word != 0) {
+        e = cudaMemsetAsync(status, 0, sizeof(int), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the no-alloc status word");
+        return la::record_error(LIN_ATTN_ERR_TIMEOUT, "a kernel of an earlier no-alloc call gave up waiting");
+    }
     return la::record_error(LIN_ATTN_OK, "");
 }

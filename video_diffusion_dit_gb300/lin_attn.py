@@ -23,7 +23,7 @@ EXPORTS = (
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
     "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward", "lin_attn_forward_fused_layout",
-    "lin_attn_set_wait_limit",
+    "lin_attn_set_wait_limit", "lin_attn_noalloc_status",
 )
 
 
@@ -47,6 +47,7 @@ def _load():
         "lin_attn_last_error": ([], ctypes.c_char_p),
         "lin_attn_version": ([], i32),
         "lin_attn_forward_noalloc": ([p, p, p, p, p, i32, i32, i64, i32, i32, p], i32),
+        "lin_attn_noalloc_status": ([p], i32),
         "lin_attn_forward_fused": ([p, p, p, p, p, p, p, i32, i64, i32, p], i32),
         "lin_attn_forward_fused_layout": ([p, p, p, p, p, p, p, i32, i64, i32, i32, p], i32),
         "lin_attn_anchor_forward": ([p, p, p, p, p, i32, i64, ctypes.c_float, p], i32),
@@ -131,6 +132,17 @@ def forward_noalloc(q_rot, k_rot, v, normalizer, out, mode="high", stream=None):
                                           out.data_ptr(), code, H, N, D, _mode(mode), _stream_handle(stream, dev))
     _check(st, "lin_attn_forward_noalloc")
     return out
+
+
+def noalloc_status(device=None, stream=None) -> int:
+    """Waits for ``stream`` and returns the status of the no-alloc calls on ``device`` since
+    the previous query (OK, or ERR_TIMEOUT if a kernel gave up waiting), clearing it."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = lib.lin_attn_noalloc_status(_stream_handle(stream, dev))
+    if st not in (OK, ERR_TIMEOUT):
+        _check(st, "lin_attn_noalloc_status")
+    return st
 
 
 class LinAttn:
