@@ -157,8 +157,14 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             const uint64_t tab_pol = policy_evict_last();
             uint32_t it = 0;
-            for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it) {
-                const HeadTile ht = split_tile(plan, t);
+            // (head, tile) of t, advanced by one per tile and recomputed where a run ends.
+            HeadTile ht{0, 0};
+            int64_t run_end = ct.t_s;
+            for (int64_t t = ct.t_s; t < ct.t_e; ++t, ++it, ++ht.tile) {
+                if (t == run_end) {
+                    ht = split_tile(plan, t);
+                    run_end = split_run_end(plan, t);
+                }
                 const int h = ht.h;
                 const int y = static_cast<int>(ht.tile * kKvTile);
                 const int c1 = token_major ? h - work.h0 : y, c2 = token_major ? y : h - work.h0;
