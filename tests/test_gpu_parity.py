@@ -236,6 +236,23 @@ def test_host_pipeline_uneven_chunks_bitwise(la, dev):
             assert ctx.device_status() == 0
 
 
+def test_host_pipeline_with_shared_tails_bitwise(la, dev):
+    """A length where the KV split hands the tails of all heads to the spare CTAs (152
+    chunks at H = 20): the host path launches one head at a time, each launch running the
+    body chunks of its head and the tail chunks that touch it, clipped to it; the partial
+    sums, so the result, must be bitwise those of the whole-layer call, in both tiers."""
+    H, N, D = 20, 120000, 112
+    assert la.kv_plan(H, N) == (152, 9)
+    g = synth.make_layer(H, N, D, 21, device=dev)
+    pinned = {k: t.cpu().pin_memory() for k, t in g.items()}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in MODES:
+            d = run(ctx, g, mode, torch.float32).cpu()
+            h = ctx.forward_host(pinned["q_rot"], pinned["k_rot"], pinned["v"], pinned["den"], mode=mode)
+            assert torch.equal(d, h), mode
+            assert ctx.device_status() == 0
+
+
 def test_out_of_range_and_misaligned_calls_are_rejected(la, dev):
     import ctypes
     g = to_dev(synth.make_layer(2, 256, 32, 0), dev)
