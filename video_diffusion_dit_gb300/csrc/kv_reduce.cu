@@ -43,13 +43,19 @@ constexpr uint32_t kKvAtomBytes = kKvTile * 128;  // one box: 64 token rows x 12
 template <int NBOX, bool FUSED>
 struct KvLayout {
     // The fused path also stages the tile's rows of the two rotation tables (FP32,
-    // [64 tokens][D/2], at most 16 KB each), so it runs with fewer, larger stages.
-    static constexpr int stages = FUSED ? 3 : kKvStages;
+    // [64 tokens][D/2], at most 16 KB each) in a ring of their own: the tables mostly come
+    // from L2 (every head reads the same rows), K and V from DRAM, so the K/V ring keeps
+    // four tiles in flight and the table ring three (a table copy is issued two tiles
+    // before its transform).
+    static constexpr int stages = FUSED ? 4 : kKvStages;
+    static constexpr int tab_ring = 3;                  // table slots of the fused kernel
+    static constexpr int tab_slots = FUSED ? tab_ring : 0;  // ... and the shared memory they take
     static constexpr uint32_t a_bytes = 2 * kKvAtomBytes;  // A = K^T: 2 atoms cover M = 128
     static constexpr uint32_t b_bytes = NBOX * kKvAtomBytes;
     static constexpr uint32_t tab_bytes = kKvTile * 64 * 4;  // one table's rows, D/2 <= 64 columns
-    static constexpr uint32_t stage_bytes = a_bytes + b_bytes + (FUSED ? 2 * tab_bytes : 0);
-    static constexpr uint32_t bar_offset = stages * stage_bytes;
+    static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+    static constexpr uint32_t tab_offset = stages * stage_bytes;  // [tab_slots][cos, sin]
+    static constexpr uint32_t bar_offset = tab_offset + tab_slots * 2 * tab_bytes;
     static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;  // + barriers + alignment slack
     // TMEM: two 128-column accumulators; the fused kernel keeps the segment's running sum in
     // a third region (columns 256..383) instead of registers, which leaves the registers to
@@ -96,6 +102,9 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     const uint32_t acc_empty0 = acc_full0 + 16u;          // [2]
     const uint32_t drain_bar = acc_empty0 + 16u;
     const uint32_t ready0 = drain_bar + 8u;               // [L::stages] (fused: tile transformed)
+    const uint32_t tab_full0 = ready0 + 8u * L::stages;   // [L::tab_slots] (fused: table rows landed)
+    const uint32_t tab_empty0 = tab_full0 + 8u * L::tab_slots;  // [L::tab_slots] (... and used)
+    static_assert(3 * L::stages * 8 + 48 + 16 * L::tab_slots <= 192, "barriers overlap the TMEM address slot");
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 200);
 
@@ -110,6 +119,10 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
             if (FUSED) mbar_init(ready0 + 8u * s, kKvTransformThreads);
+        }
+        for (int s = 0; s < L::tab_slots; ++s) {
+            mbar_init(tab_full0 + 8u * s, 1);
+            mbar_init(tab_empty0 + 8u * s, kKvTransformThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             // other CTAs read at about the same time: those lines stay at normal priority.
             const uint64_t pol = token_major ? policy_evict_normal() : policy_evict_first();
             const uint64_t tab_pol = policy_evict_last();
-            uint32_t it = 0;
+            uint32_t it = 0, n_tab = 0;  // K/V loads issued; table loads issued (fused)
             // (head, tile) of t, advanced by one per tile and recomputed where a run ends.
             HeadTile ht{0, 0};
             int64_t run_end = ct.t_s;
@@ -172,26 +185,39 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                 if (!mbar_wait(empty0 + 8u * st, ph ^ 1u, abort_flag, status, wait_ns)) break;
                 const uint32_t a = base + st * L::stage_bytes;
                 const uint32_t b = a + L::a_bytes;
-                const uint32_t tab_tx = FUSED ? 2u * kKvTile * (head_dim / 2) * 4u : 0u;
-                mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes + tab_tx);
+                mbar_arrive_expect_tx(full0 + 8u * st, 2u * NBOX * kKvAtomBytes);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x) {
                     tma_load_3d_hint(a + x * kKvAtomBytes, &tm_k, full0 + 8u * st, 64 * x, c1, c2, pol);
                     tma_load_3d_hint(b + x * kKvAtomBytes, &tm_v, full0 + 8u * st, 64 * x, c1, c2, pol);
                 }
-                if (FUSED) {
-                    // rotation-table rows of the tile's tokens (kept in L2: every head re-reads them)
-                    const uint32_t tab = b + L::b_bytes;
-                    tma_load_2d_hint(tab, &tm_cos, full0 + 8u * st, 0, y, tab_pol);
-                    tma_load_2d_hint(tab + L::tab_bytes, &tm_sin, full0 + 8u * st, 0, y, tab_pol);
+                if constexpr (FUSED) {
+                    // Rotation-table rows of the tile's tokens (kept in L2: every head re-reads
+                    // them), into the table slot the transform of tile it - tab_slots freed.
+                    const uint32_t ts = it % L::tab_slots, tpar = (it / L::tab_slots) & 1u;
+                    if (!mbar_wait(tab_empty0 + 8u * ts, tpar ^ 1u, abort_flag, status, wait_ns)) {
+                        ++it;  // this tile's K/V loads were issued
+                        break;
+                    }
+                    const uint32_t tab = base + L::tab_offset + ts * 2u * L::tab_bytes;
+                    mbar_arrive_expect_tx(tab_full0 + 8u * ts, 2u * kKvTile * (head_dim / 2) * 4u);
+                    tma_load_2d_hint(tab, &tm_cos, tab_full0 + 8u * ts, 0, y, tab_pol);
+                    tma_load_2d_hint(tab + L::tab_bytes, &tm_sin, tab_full0 + 8u * ts, 0, y, tab_pol);
+                    ++n_tab;
                 }
             }
             // Let the loads already issued land before shared memory goes away: the MMA
-            // issuer waits for all of them unless some role gave up, in which case nothing
-            // else would.  (`it` loads were issued; only the last `stages` can be pending.)
+            // issuer and the transform wait for all of them unless some role gave up, in which
+            // case nothing else would.  (`it` K/V loads and `n_tab` table loads were issued;
+            // only the last `stages` / `tab_slots` of each can be pending.)
             const uint32_t first = it > L::stages ? it - L::stages : 0;
             for (uint32_t j = first; j < it; ++j)
                 mbar_wait_drain(full0 + 8u * (j % L::stages), (j / L::stages) & 1u);
+            if constexpr (FUSED) {
+                const uint32_t first_tab = n_tab > L::tab_slots ? n_tab - L::tab_slots : 0;
+                for (uint32_t j = first_tab; j < n_tab; ++j)
+                    mbar_wait_drain(tab_full0 + 8u * (j % L::tab_slots), (j / L::tab_slots) & 1u);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -259,7 +285,12 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             for (int e = 0; e < 4; ++e) ks[e] = kc[e] = 0ull;
             for (; t < seg_end; ++t, ++it) {
                 const uint32_t st = it % L::stages, ph = (it / L::stages) & 1u;
-                if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status, wait_ns)) {
+                const uint32_t tslot = it % L::tab_ring, tpar = (it / L::tab_ring) & 1u;
+                // Every transform thread waits for both the K/V stage and the table slot (also
+                // the threads with no columns to turn): the table ring is shorter than the K/V
+                // ring, so only a thread that has seen a slot's rows land may free it again.
+                if (!mbar_wait(full0 + 8u * st, ph, abort_flag, status, wait_ns) ||
+                    !mbar_wait(tab_full0 + 8u * tslot, tpar, abort_flag, status, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -269,7 +300,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     // and add zero to the sums, so every row is transformed without a test.
                     uint8_t* stage = base_ptr + st * L::stage_bytes;
                     uint8_t* atom = stage + (c >> 3) * kKvAtomBytes;
-                    const uint8_t* tab = stage + L::a_bytes + L::b_bytes + 16 * c;  // [64][pairs] floats
+                    const uint8_t* tab = base_ptr + L::tab_offset + tslot * 2u * L::tab_bytes + 16 * c;  // [64][pairs]
                     uint64_t ts[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                     for (int k = 0; k < kKvTile / kKsumGroups; ++k) {
@@ -297,6 +328,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     }
                 }
                 fence_proxy_async_smem();
+                mbar_arrive(tab_empty0 + 8u * tslot);
                 mbar_arrive(ready0 + 8u * st);
             }
             if (!ok) break;
