@@ -64,6 +64,9 @@ struct KvLayout {
     static constexpr uint32_t sum_col = 256;
 };
 
+static_assert(KvLayout<2, true>::smem_bytes <= 232448 && KvLayout<2, false>::smem_bytes <= 232448,
+              "KV layout exceeds the 227 KB of shared memory a CTA may use");
+
 // Virtual tiles [t_s, t_e) of the CTA's chunk (see TileSplit), clipped to the launch's heads.
 struct ChunkTiles {
     int64_t c, t_s, t_e;
