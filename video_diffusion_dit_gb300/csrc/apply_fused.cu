@@ -41,7 +41,6 @@ constexpr int kFXfWarps = 16;                       // warps 10..25
 constexpr int kFXfWarp0 = 2 + kFEpiWarps;
 constexpr int kFThreads = 32 * (kFXfWarp0 + kFXfWarps);
 constexpr int kFTransformThreads = 32 * kFXfWarps;
-constexpr int kFRowGroups = kFTransformThreads / 16;  // a transform thread takes rows rg + kFRowGroups k
 constexpr int kFTabSubs = 2;                        // table slots per tile (half a tile of rows each)
 constexpr int kFTabSlots = 3 * kFTabSubs / 2;       // table ring: 1.5 tiles of rows
 constexpr uint32_t kFOutBufs = 1;                   // staging buffers per epilogue warp
@@ -73,7 +72,6 @@ static_assert(fused_smem_bytes(128) <= kFSmemLimit && fused_smem_bytes(64) <= kF
 static_assert(kFImgCol + 3 * 64 <= 512, "accumulators and image exceed TMEM");
 static_assert((3 * fused_stages(1) + 4 + 2 * kFDenBufs + 2 * kFTabSlots + 3) * 8 <= kFBarBytes - 64,
               "barriers overlap the TMEM address slot");
-static_assert(kFTabRows % (kFXfWarps * 32 / 16) == 0, "a table slot must hold whole row groups");
 
 template <int NBOX, bool OUT_BF16>
 __global__ void __launch_bounds__(kFThreads, 1)
@@ -256,13 +254,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
     } else if (warp >= kFXfWarp0) {
         // ---------------- producer-step transform of the Q tiles
-        // Thread (chunk c, row group rg) takes columns 8c..8c+7 of rows rg + 32 k, k = 0..3:
+        // Thread (chunk c, row group rg) takes columns 8c..8c+7 of rows rg + G k, with
+        // kCpr = 16 chunk lanes per row and G = 32 row groups (4 rows a thread) when the head
+        // dim spans two 64-column atoms, 8 lanes and 64 groups (2 rows) when it fits one:
         // ReLU, dot with the head's column sums of relu(K) (the normaliser), then the rotation
-        // (binary32 products and sum in a fixed order, rounded once to BF16).  The 16 threads of
+        // (binary32 products and sum in a fixed order, rounded once to BF16).  The threads of
         // a row add their dot products in a fixed butterfly; the row's reciprocal denominator
         // (correctly rounded) goes to rcp_s for the epilogue.
+        constexpr int kCpr = 8 * NBOX;                   // chunk lanes per row
+        constexpr int kRowGroups = kFTransformThreads / kCpr;
+        static_assert(kFTabRows % kRowGroups == 0, "a table slot must hold whole row groups");
         const int u = threadIdx.x - 32 * kFXfWarp0;
-        const int c = u & 15, rg = u >> 4;
+        const int c = u % kCpr, rg = u / kCpr;
         const bool live = 8 * c < head_dim;
         const uint32_t row_bytes = half_d * 4u;
         uint64_t ks[4];  // the head's column sums in rope_chunk's activation order
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const uint32_t slot = i % kFTabSlots;
                 if (!(ok = mbar_wait(tab_full0 + 8u * slot, (i / kFTabSlots) & 1u, abort_flag, status, wait_ns))) break;
                 const uint8_t* tab = base_ptr + (tab_smem - base) + slot * tab_slot + 16 * c;
-                constexpr int kPer = kFTabRows / kFRowGroups;  // this thread's rows per slot
+                constexpr int kPer = kFTabRows / kRowGroups;  // this thread's rows per slot
                 float part[kPer];
                 if (live) {
                     // All of the slot's loads first, then the arithmetic: the rows' chains overlap.
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     float4 c4[kPer], s4[kPer];
 #pragma unroll
                     for (int kk = 0; kk < kPer; ++kk) {
-                        const int r = rg + kFRowGroups * (kPer * hh + kk);
+                        const int r = rg + kRowGroups * (kPer * hh + kk);
                         const uint32_t tr = static_cast<uint32_t>(r - hh * kFTabRows) * row_bytes;
                         cell[kk] = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                         w[kk] = *cell[kk];
@@ -334,12 +337,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 }
 #pragma unroll
                 for (int kk = 0; kk < kPer; ++kk) {
-                    const int r = rg + kFRowGroups * (kPer * hh + kk);
+                    const int r = rg + kRowGroups * (kPer * hh + kk);
                     float p = part[kk];
-                    p += __shfl_xor_sync(0xffffffffu, p, 8);
-                    p += __shfl_xor_sync(0xffffffffu, p, 4);
-                    p += __shfl_xor_sync(0xffffffffu, p, 2);
-                    p += __shfl_xor_sync(0xffffffffu, p, 1);
+#pragma unroll
+                    for (int m = kCpr / 2; m >= 1; m >>= 1) p += __shfl_xor_sync(0xffffffffu, p, m);
                     if (c == 0) rcp_s[db * kApplyTile + r] = __frcp_rn(p + kDenEps);
                 }
                 mbar_arrive(tab_empty0 + 8u * slot);

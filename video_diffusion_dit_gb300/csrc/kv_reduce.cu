@@ -30,10 +30,11 @@ namespace {
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
 constexpr int kKvThreads = 192;
-constexpr int kKvThreadsFused = 192 + 32 * kKsumGroups / 2;  // + warps 6..13: the producer-step transform
-constexpr int kKvTransformThreads = kKvThreadsFused - 192;
-static_assert(kKvTransformThreads == 16 * kKsumGroups && kKvTile % kKsumGroups == 0,
-              "transform thread (chunk, row group) covers rows rg + kKsumGroups k of every tile");
+constexpr int kKvTransformThreads = 256;  // warps 6..13: the producer-step transform
+constexpr int kKvThreadsFused = 192 + kKvTransformThreads;
+static_assert(kKvTransformThreads == 16 * ksum_groups(128) && kKvTransformThreads == 8 * ksum_groups(64) &&
+                  kKvTile % ksum_groups(64) == 0 && kKvTile % ksum_groups(128) == 0,
+              "transform thread (chunk, row group) covers rows rg + groups k of every tile");
 // Tiles per tensor-core sub-chunk before its sum is promoted into FP32 registers: 4 (256
 // tokens) in the 'high' tier, 1 (64 tokens) in the 'lossless' tier.
 constexpr int kPromoteHigh = 4;
@@ -270,8 +271,10 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
         }
     } else if (FUSED && warp >= 6) {
         // ---------------- producer-step transform of the K tiles (fused path)
+        constexpr int kCpr = 8 * NBOX;                       // chunk lanes per row
+        constexpr int kGroups = kKvTransformThreads / kCpr;  // = ksum_groups(head_dim)
         const int u = threadIdx.x - 192;
-        const int c = u & 15, rg = u >> 4;
+        const int c = u % kCpr, rg = u / kCpr;
         const bool live = 8 * c < head_dim;
         const int64_t pairs = head_dim / 2;
         uint32_t it = 0;
@@ -306,8 +309,8 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
                     const uint8_t* tab = base_ptr + L::tab_offset + tslot * 2u * L::tab_bytes + 16 * c;  // [64][pairs]
                     uint64_t ts[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int k = 0; k < kKvTile / kKsumGroups; ++k) {
-                        const int r = rg + kKsumGroups * k;
+                    for (int k = 0; k < kKvTile / kGroups; ++k) {
+                        const int r = rg + kGroups * k;
                         {
                             uint4* cell = reinterpret_cast<uint4*>(atom + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                             uint4 w = *cell;
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
             // reduction adds the row groups in order, then the segments).
             if (live) {
                 const int64_t slot = static_cast<int64_t>(h) * plan.seg_stride + segment_of(plan, h, ct.c);
-                double* dst = pa.ksum_partial + (slot * kKsumGroups + rg) * head_dim + 8 * c;
+                double* dst = pa.ksum_partial + (slot * kGroups + rg) * head_dim + 8 * c;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float s0, s1, c0, c1;
@@ -484,16 +487,27 @@ __device__ __forceinline__ float reduce_segments(const float* p, int64_t stride,
 }
 
 // Fixed-order sum of a head's FP64 column-sum partials (fused path): each segment's value
-// is its row-group sums added in order (p[s][0..kKsumGroups-1], `stride` apart), then the
+// is its row-group sums added in order (p[s][0..groups-1], `stride` apart), then the
 // segments are added with the same tree as above.
-__device__ __forceinline__ double segment_value_f64(const double* p, int64_t stride, int s) {
-    const double* q = p + static_cast<int64_t>(s) * kKsumGroups * stride;
+__device__ __forceinline__ double segment_value_f64(const double* p, int64_t stride, int s, int groups) {
+    const double* q = p + static_cast<int64_t>(s) * groups * stride;
     double v = q[0];
-#pragma unroll
-    for (int g = 1; g < kKsumGroups; ++g) v += q[g * stride];
+    for (int g = 1; g < groups; ++g) v += q[g * stride];
     return v;
 }
-__device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t stride, int nseg) {
+// The same value with every load issued before the first add (one thread per segment).
+__device__ __forceinline__ double segment_value_f64_wide(const double* p, int64_t stride, int s, int groups) {
+    const double* q = p + static_cast<int64_t>(s) * groups * stride;
+    double x[kKsumGroupsMax];
+#pragma unroll
+    for (int g = 0; g < kKsumGroupsMax; ++g) x[g] = g < groups ? q[g * stride] : 0.0;
+    double v = x[0];
+#pragma unroll
+    for (int g = 1; g < kKsumGroupsMax; ++g)
+        if (g < groups) v += x[g];
+    return v;
+}
+__device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t stride, int nseg, int row_groups) {
     double groups[kTreeGroups];
     int ngroups = 0;
 #pragma unroll
@@ -503,7 +517,7 @@ __device__ __forceinline__ double reduce_segments_f64(const double* p, int64_t s
         if (g0 < nseg) {
             double vals[kTreeGroup];
 #pragma unroll
-            for (int s = 0; s < kTreeGroup; ++s) vals[s] = g0 + s < nseg ? segment_value_f64(p, stride, g0 + s) : 0.0;
+            for (int s = 0; s < kTreeGroup; ++s) vals[s] = g0 + s < nseg ? segment_value_f64(p, stride, g0 + s, row_groups) : 0.0;
 #pragma unroll
             for (int w = 1; w < kTreeGroup; w *= 2)
 #pragma unroll
@@ -577,10 +591,11 @@ __global__ void __launch_bounds__(256, 2) kv_finalize_kernel(const float* partia
     if (ksum_partial != nullptr) {
         // Fused path: the column sums of relu(K) of columns 8r .. 8r+7 over all tokens, each
         // segment's row groups in order, then the segments in the same tree; rounded once to FP32.
-        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * kKsumGroups * head_dim;
+        const int groups = ksum_groups(head_dim);
+        const double* kp = ksum_partial + static_cast<int64_t>(h) * plan.seg_stride * groups * head_dim;
         const int t = threadIdx.x;
         if constexpr (SMALL) {
-            if (t < 8 * nseg) ks_seg[t >> 3][t & 7] = segment_value_f64(kp + 8 * r + (t & 7), head_dim, t >> 3);
+            if (t < 8 * nseg) ks_seg[t >> 3][t & 7] = segment_value_f64_wide(kp + 8 * r + (t & 7), head_dim, t >> 3, groups);
             __syncthreads();
             if (t < 8) {
                 double vals[kSmallSegs];
@@ -594,7 +609,7 @@ __global__ void __launch_bounds__(256, 2) kv_finalize_kernel(const float* partia
                 ksum[h * head_dim + 8 * r + t] = static_cast<float>(vals[0]);
             }
         } else if (t < 8) {
-            ksum[h * head_dim + 8 * r + t] = static_cast<float>(reduce_segments_f64(kp + 8 * r + t, head_dim, nseg));
+            ksum[h * head_dim + 8 * r + t] = static_cast<float>(reduce_segments_f64(kp + 8 * r + t, head_dim, nseg, groups));
         }
     }
     if (image == nullptr) return;

@@ -339,7 +339,7 @@ int lin_attn_create(lin_attn_ctx** out_ctx, int heads, int64_t max_tokens, int h
                 cudaMalloc(&c->kv, sizeof(float) * dd * heads) == cudaSuccess &&
                 cudaMalloc(&c->kv_image, static_cast<size_t>(la::kv_image_bytes(head_dim)) * heads) == cudaSuccess &&
                 cudaMalloc(&c->status, sizeof(int)) == cudaSuccess &&
-                cudaMalloc(&c->ksum_partial, sizeof(double) * heads * c->seg_stride_alloc * la::kKsumGroups * head_dim) ==
+                cudaMalloc(&c->ksum_partial, sizeof(double) * heads * c->seg_stride_alloc * la::kKsumGroupsMax * head_dim) ==
                     cudaSuccess &&
                 cudaMalloc(&c->ksum, sizeof(float) * heads * head_dim) == cudaSuccess;
     if (!good) {

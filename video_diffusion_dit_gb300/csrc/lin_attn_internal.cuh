@@ -264,11 +264,14 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
 // The producer step fused into the tensor-core kernels (ReLU + interleaved RoPE on the
 // loaded Q / K tiles, the normaliser from the activated un-rotated copies).
 //   cos, sin : FP32 [N][D/2] rotation tables (pair p of token n is turned by cos/sin[n][p])
-//   ksum_partial : FP64 [H][seg_stride][kKsumGroups][D] per-chunk, per-row-group column
+//   ksum_partial : FP64 [H][seg_stride][ksum_groups(D)][D] per-chunk, per-row-group column
 //                  sums of relu(K) (scratch)
 //   ksum : FP32 [H][D] reduced column sums (scratch; read by the apply)
-// Row groups of the fused KV kernel's transform (one column-sum partial each).
-constexpr int kKsumGroups = 16;
+// Row groups of the fused KV kernel's transform (one column-sum partial each): its 256
+// threads are 16 chunk lanes x 16 row groups when the head dim spans two 64-column atoms,
+// 8 lanes x 32 groups when it fits one.
+__host__ __device__ constexpr int ksum_groups(int head_dim) { return head_dim <= 64 ? 32 : 16; }
+constexpr int kKsumGroupsMax = 32;
 struct ProducerArgs {
     const float* cos;
     const float* sin;
