@@ -13,8 +13,9 @@
 // The KV image (KV^T split into three BF16 terms hi + mid + lo, which carry 24 bits of KV,
 // so every product is exact in FP32 and the result has FP32-class accuracy) lives in TMEM
 // as the A operand of tcgen05.mma, which leaves shared memory to the streams: Q tiles, the
-// rotation-table rows and the output staging.  Per CTA (persistent; k CTAs per head, each
-// a contiguous range of one head's tiles, every head cut at the same tiles):
+// rotation-table rows and the output staging.  Per CTA (persistent; one chunk of the body +
+// tail split: k CTAs per head on the first B tiles of every head, cut at the same tiles,
+// and the spare CTAs on the remaining tiles of all heads):
 //   warp 0      TMA Q tiles (K-major, 128-byte swizzle: the B operand as loaded) and
 //               bulk-copies each half tile's table rows into a three-slot ring;
 //   warp 1      3 terms x D/16 K-steps of tcgen05.mma M=128 (features) N=128 (tokens) into

@@ -9,10 +9,12 @@
 // GEMM on BF16 operands is the FP32 GEMM on the upcast operands up to rounding; 'lossless'
 // promotes the tensor-core sums into FP32 registers four times as often.
 //
-// Work split (KvPlan): each head's 64-token tiles are cut into k equal contiguous chunks,
-// at the same token boundaries for every head, one CTA each.  A chunk leaves one D x D
-// partial sum (a "segment"); kv_finalize adds each head's partials in a fixed pairwise
-// order.  k depends on the shape alone, and so do the order and the result.
+// Work split (KvPlan, lin_attn_internal.cuh): k chunks per head on the first B of each
+// head's 64-token tiles, cut at the same token boundaries for every head, and on long
+// sequences the spare chunks (152 - k H) on the remaining tiles of all heads; one CTA per
+// chunk.  Each run of a chunk within one head (a "segment") leaves one D x D partial sum;
+// kv_finalize adds each head's partials in a fixed pairwise order.  The split depends on
+// the shape alone, and so do the order and the result.
 #include <cuda_bf16.h>
 
 #include "lin_attn_internal.cuh"
@@ -24,8 +26,9 @@ namespace {
 // ============================================================================ tensor cores
 // Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma, warps 2..5 drain the
 // TMEM accumulator; the fused-producer instantiation adds warps 6..13, which turn each
-// loaded K tile into relu(K) rotated (in place) and sum the columns of relu(K).  Per stage, one 64-token tile of K and of V is loaded with 128-byte
-// swizzle as [token][64 head-dim columns] boxes - exactly the MN-major canonical layout of
+// loaded K tile into relu(K) rotated (in place) and sum the columns of relu(K).  Per
+// stage, one 64-token tile of K and of V is loaded with 128-byte swizzle as
+// [token][64 head-dim columns] boxes - exactly the MN-major canonical layout of
 // the MMA operands A = K^T (M = head-dim row i) and B = V (N = head-dim column j), with
 // K = tokens.  M is always 128 (head dims up to 128; rows i >= D are zero).
 constexpr int kKvStages = 6;
