@@ -33,20 +33,27 @@ constexpr int kApplyEpiWarps = 8;
 constexpr int kApplyThreads = 32 * (2 + kApplyEpiWarps);
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
 constexpr uint32_t kOutBoxBytes = 32 * 128;         // 32 rows x 128 bytes
-__host__ __device__ constexpr uint32_t apply_out_bufs(int nbox) { return nbox == 1 ? 2u : 1u; }
 constexpr uint32_t kApplyBarBytes = 512;            // mbarriers, TMEM address, abort flag
 constexpr uint32_t kSmemLimit = 232448;
 
-// Q stages: a one-atom tile (D <= 64) is half the bytes, so twice the stages keep as many
-// bytes in flight.
-__host__ __device__ constexpr int apply_stages(int nbox) { return nbox == 1 ? 6 : 3; }
-
-__host__ __device__ constexpr uint32_t apply_smem_bytes(int head_dim) {
-    return static_cast<uint32_t>(kv_image_bytes(head_dim)) +
-           apply_stages(head_dim_atoms(head_dim)) * head_dim_atoms(head_dim) * kQAtomBytes +
-           kApplyEpiWarps * apply_out_bufs(head_dim_atoms(head_dim)) * kOutBoxBytes + kApplyBarBytes + 1024;
+// Shared memory beside the KV image goes to Q stages and output staging.  A one-atom tile
+// (D <= 64) is half the bytes, so it gets twice the stages.  With FP32 output and two atoms
+// the output is twice the bytes of Q and the staging is what paces the epilogue: two Q
+// stages and two staging buffers per warp (0.4055 -> 0.3874 ms at 720p) rather than three
+// and one; BF16 output keeps three and one (two and two: 0.2780 -> 0.2805 ms).  At D <= 64
+// a third staging buffer per warp changed nothing (0.4118 / 0.4121 ms).
+__host__ __device__ constexpr int apply_stages(int nbox, bool bf16) { return nbox == 1 ? 6 : (bf16 ? 3 : 2); }
+__host__ __device__ constexpr uint32_t apply_out_bufs(int nbox, bool bf16) {
+    return nbox == 1 ? 2u : (bf16 ? 1u : 2u);
 }
-static_assert(apply_smem_bytes(128) <= kSmemLimit && apply_smem_bytes(64) <= kSmemLimit,
+
+__host__ __device__ constexpr uint32_t apply_smem_bytes(int head_dim, bool bf16) {
+    return static_cast<uint32_t>(kv_image_bytes(head_dim)) +
+           apply_stages(head_dim_atoms(head_dim), bf16) * head_dim_atoms(head_dim) * kQAtomBytes +
+           kApplyEpiWarps * apply_out_bufs(head_dim_atoms(head_dim), bf16) * kOutBoxBytes + kApplyBarBytes + 1024;
+}
+static_assert(apply_smem_bytes(128, false) <= kSmemLimit && apply_smem_bytes(64, false) <= kSmemLimit &&
+                  apply_smem_bytes(128, true) <= kSmemLimit && apply_smem_bytes(64, true) <= kSmemLimit,
               "apply layout exceeds shared memory");
 
 template <int NBOX, bool OUT_BF16>
@@ -59,13 +66,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
 
-    constexpr int kApplyStages = apply_stages(NBOX);
+    constexpr int kApplyStages = apply_stages(NBOX, OUT_BF16);
     const uint32_t img_bytes = 3u * NBOX * head_dim * 128u;
     const uint32_t term_bytes = NBOX * head_dim * 128u;
     const uint32_t b_smem = base;
     const uint32_t q_smem = b_smem + img_bytes;
     const uint32_t o_smem = q_smem + kApplyStages * NBOX * kQAtomBytes;
-    constexpr uint32_t kOutBufs = apply_out_bufs(NBOX);
+    constexpr uint32_t kOutBufs = apply_out_bufs(NBOX, OUT_BF16);
     const uint32_t bar_off = o_smem + kApplyEpiWarps * kOutBufs * kOutBoxBytes - base;
     const uint32_t bars = base + bar_off;
     const uint32_t q_full0 = bars;                        // [kApplyStages]
@@ -307,7 +314,7 @@ template <int NBOX, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
                       int heads, int n_tokens, int head_dim, bool token_major, const TileSplit& sp, int grid,
                       int* status, uint64_t wait_ns, cudaStream_t stream) {
-    const uint32_t smem = apply_smem_bytes(head_dim);
+    const uint32_t smem = apply_smem_bytes(head_dim, BF16);
     cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
