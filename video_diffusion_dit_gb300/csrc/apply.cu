@@ -77,9 +77,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
     const uint32_t bars = base + bar_off;
     const uint32_t q_full0 = bars;                        // [kApplyStages]
     const uint32_t q_empty0 = bars + 8u * kApplyStages;   // [kApplyStages]
-    const uint32_t acc_full0 = bars + 16u * kApplyStages; // [2]
-    const uint32_t acc_empty0 = acc_full0 + 16u;          // [2]
-    const uint32_t b_full = acc_empty0 + 16u;
+    // TMEM accumulators (N = D columns each, in 256 allocated columns): two of 128 columns, or
+    // four of 64 when D <= 64, so that the MMA can run further ahead of the epilogue there.
+    constexpr uint32_t kAcc = NBOX == 1 ? 4u : 2u;
+    constexpr uint32_t kAccCols = 256u / kAcc;
+    static_assert((2 * kApplyStages + 2 * kAcc + 3) * 8 <= kApplyBarBytes - 64, "barriers overlap the TMEM address slot");
+    const uint32_t acc_full0 = bars + 16u * kApplyStages; // [kAcc]
+    const uint32_t acc_empty0 = acc_full0 + 8u * kAcc;    // [kAcc]
+    const uint32_t b_full = acc_empty0 + 8u * kAcc;
     const uint32_t b_empty = b_full + 8u;
     const uint32_t drain_bar = b_empty + 8u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + bar_off + kApplyBarBytes - 64);
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             mbar_init(q_full0 + 8u * s, 1);
             mbar_init(q_empty0 + 8u * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (uint32_t b = 0; b < kAcc; ++b) {
             mbar_init(acc_full0 + 8u * b, 1);
             mbar_init(acc_empty0 + 8u * b, kApplyEpiWarps);
         }
@@ -198,13 +203,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
                     if (!mbar_wait(b_full, run & 1, abort_flag, status, wait_ns)) break;
                     tc_fence_after();
                 }
-                const uint32_t buf = lt & 1u;
-                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt >> 1) & 1u) ^ 1u, abort_flag, status, wait_ns)) break;
+                const uint32_t buf = lt % kAcc;
+                if (!mbar_wait(acc_empty0 + 8u * buf, ((lt / kAcc) & 1u) ^ 1u, abort_flag, status, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t st = it % kApplyStages, ph = (it / kApplyStages) & 1u;
                 if (!mbar_wait(q_full0 + 8u * st, ph, abort_flag, status, wait_ns)) break;
                 tc_fence_after();
-                const uint32_t d = tmem + buf * 128u;
+                const uint32_t d = tmem + buf * kAccCols;
                 const uint32_t qa = q_smem + st * NBOX * kQAtomBytes;
                 // Smallest term first; every product is exact, the accumulator is FP32.
 #pragma unroll
@@ -245,12 +250,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
             const uint32_t lt = static_cast<uint32_t>(t - t_begin);
             const int row0 = n0 + 32 * q;
             const int row = row0 + lane;
-            const uint32_t buf = lt & 1u;
+            const uint32_t buf = lt % kAcc;
             const float dv = row < n_tokens ? den[static_cast<int64_t>(h) * n_tokens + row] : 1.0f;
             const float rcp = __frcp_rn(dv);
-            if (!mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns)) break;
+            if (!mbar_wait(acc_full0 + 8u * buf, (lt / kAcc) & 1u, abort_flag, status, wait_ns)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * 128u;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + buf * kAccCols;
             // A warp whose 32 rows all lie past the end of the head (ragged last tile) has
             // nothing to store.  It must not touch its staging buffers either: every buffer
             // write is paired with one committed store, which is what lets wait_group.read 1
