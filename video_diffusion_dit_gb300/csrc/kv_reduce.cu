@@ -51,12 +51,12 @@ struct KvLayout {
     // from L2 (every head reads the same rows), K and V from DRAM, so the K/V ring keeps
     // four tiles in flight and the table ring three (a table copy is issued two tiles
     // before its transform).
-    static constexpr int stages = FUSED ? 4 : kKvStages;
+    static constexpr int stages = FUSED ? (NBOX == 1 ? 6 : 4) : kKvStages;
     static constexpr int tab_ring = 3;                  // table slots of the fused kernel
     static constexpr int tab_slots = FUSED ? tab_ring : 0;  // ... and the shared memory they take
     static constexpr uint32_t a_bytes = 2 * kKvAtomBytes;  // A = K^T: 2 atoms cover M = 128
     static constexpr uint32_t b_bytes = NBOX * kKvAtomBytes;
-    static constexpr uint32_t tab_bytes = kKvTile * 64 * 4;  // one table's rows, D/2 <= 64 columns
+    static constexpr uint32_t tab_bytes = kKvTile * 32 * NBOX * 4;  // one table's rows, D/2 <= 32 NBOX columns
     static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
     static constexpr uint32_t tab_offset = stages * stage_bytes;  // [tab_slots][cos, sin]
     static constexpr uint32_t bar_offset = tab_offset + tab_slots * 2 * tab_bytes;
@@ -68,7 +68,8 @@ struct KvLayout {
     static constexpr uint32_t sum_col = 256;
 };
 
-static_assert(KvLayout<2, true>::smem_bytes <= 232448 && KvLayout<2, false>::smem_bytes <= 232448,
+static_assert(KvLayout<2, true>::smem_bytes <= 232448 && KvLayout<2, false>::smem_bytes <= 232448 &&
+                  KvLayout<1, true>::smem_bytes <= 232448 && KvLayout<1, false>::smem_bytes <= 232448,
               "KV layout exceeds the 227 KB of shared memory a CTA may use");
 
 // Virtual tiles [t_s, t_e) of the CTA's chunk (see TileSplit), clipped to the launch's heads.
@@ -111,9 +112,9 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     const uint32_t ready0 = drain_bar + 8u;               // [L::stages] (fused: tile transformed)
     const uint32_t tab_full0 = ready0 + 8u * L::stages;   // [L::tab_slots] (fused: table rows landed)
     const uint32_t tab_empty0 = tab_full0 + 8u * L::tab_slots;  // [L::tab_slots] (... and used)
-    static_assert(3 * L::stages * 8 + 48 + 16 * L::tab_slots <= 192, "barriers overlap the TMEM address slot");
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 200);
+    static_assert(3 * L::stages * 8 + 40 + 16 * L::tab_slots <= 240, "barriers overlap the TMEM address slot");
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 240);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 248);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
