@@ -333,20 +333,21 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
 template <int NBOX, bool BF16>
 cudaError_t launch_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* img, const float* den,
                       int heads, int n_tokens, int head_dim, bool token_major, const TileSplit& sp, int grid,
-                      int* status, uint64_t wait_ns, cudaStream_t stream) {
+                      int* status, uint64_t wait_ns, cudaStream_t stream, bool overlap) {
     const uint32_t smem = apply_smem_bytes(head_dim, BF16);
     cudaError_t e = cudaFuncSetAttribute(apply_tc_kernel<NBOX, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_overlapped(apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q, tm_out,
-                             img, den, heads, n_tokens, head_dim, sp, token_major ? 1 : 0, status, wait_ns);
+    return launch_kernel(overlap, apply_tc_kernel<NBOX, BF16>, dim3(grid), dim3(kApplyThreads), smem, stream, tm_q,
+                         tm_out, img, den, heads, n_tokens, head_dim, sp, token_major ? 1 : 0, status, wait_ns);
 }
 
 }  // namespace
 
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream) {
+                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream,
+                            bool overlap) {
     const int n = static_cast<int>(n_tokens);
     const int tph = (n + kApplyTile - 1) / kApplyTile;
     const int total = heads * tph;
@@ -360,7 +361,8 @@ cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, 
     }
     const bool one = head_dim_atoms(head_dim) == 1;
 #define LA_APPLY(NB, BF) \
-    launch_tc<NB, BF>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, sp, grid, status, wait_ns, stream)
+    launch_tc<NB, BF>(tm_q, tm_out, kv_image, den, heads, n, head_dim, token_major, sp, grid, status, wait_ns, stream, \
+                      overlap)
     if (one) return out_bf16 ? LA_APPLY(1, true) : LA_APPLY(1, false);
     return out_bf16 ? LA_APPLY(2, true) : LA_APPLY(2, false);
 #undef LA_APPLY

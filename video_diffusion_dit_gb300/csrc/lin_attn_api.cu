@@ -35,7 +35,7 @@ struct lin_attn_ctx {
     // host-buffer pipeline: copy streams and ordering events, created on first use
     cudaStream_t s_in = nullptr;
     cudaStream_t s_out = nullptr;
-    cudaEvent_t ev_ready = nullptr, ev_in = nullptr, ev_comp = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_ready = nullptr, ev_kv = nullptr, ev_in = nullptr, ev_comp = nullptr, ev_done = nullptr;
     // timing hook (one-shot)
     cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
     int n_events = 0;
@@ -157,7 +157,7 @@ void free_all(lin_attn_ctx* c) {
     cudaFree(c->st_out);
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
-    for (cudaEvent_t ev : {c->ev_ready, c->ev_in, c->ev_comp, c->ev_done})
+    for (cudaEvent_t ev : {c->ev_ready, c->ev_kv, c->ev_in, c->ev_comp, c->ev_done})
         if (ev) cudaEventDestroy(ev);
 }
 
@@ -182,7 +182,7 @@ int check_call(const lin_attn_ctx* ctx, const void* q, const void* k, const void
 int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, const float* den, void* out,
                   int out_dtype, int64_t n_tokens, int mode, cudaStream_t stream, int h0, int hc,
                   cudaEvent_t* ev, int layout = LIN_ATTN_LAYOUT_HND, const float* rope_cos = nullptr,
-                  const float* rope_sin = nullptr) {
+                  const float* rope_sin = nullptr, cudaEvent_t apply_after = nullptr) {
     const int H = c->heads, D = c->head_dim;
     const bool bf16_out = out_dtype == LIN_ATTN_OUT_BF16;
     const bool lossless = mode == LIN_ATTN_MODE_LOSSLESS;
@@ -227,6 +227,11 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
     e = la::launch_kv_finalize(c->partial, c->kv, c->kv_image, h0, hc, D, plan, stream, fused ? &pa_kv : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kv_finalize launch");
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    // (host-buffer pipeline: Q and the denominators may still be on their way when the KV
+    // kernels start; the apply, which fetches Q before its grid-dependency wait, is then
+    // launched without the overlap so that it cannot start before they land)
+    if (apply_after && (e = cudaStreamWaitEvent(stream, apply_after, 0)) != cudaSuccess)
+        return cuda_fail(e, "stream ordering");
     {
         CUtensorMap tq, to;
         int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
@@ -244,7 +249,7 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
             if (rc) return rc;
             e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, c->wait_ns,
-                                    stream);
+                                    stream, apply_after == nullptr);
         }
         if (e != cudaSuccess) return cuda_fail(e, "apply_tc launch");
     }
@@ -487,7 +492,7 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
         if ((e = cudaStreamCreateWithFlags(&ctx->s_in, cudaStreamNonBlocking)) != cudaSuccess ||
             (e = cudaStreamCreateWithFlags(&ctx->s_out, cudaStreamNonBlocking)) != cudaSuccess)
             return cuda_fail(e, "cudaStreamCreate");
-        for (cudaEvent_t* ev : {&ctx->ev_ready, &ctx->ev_in, &ctx->ev_comp, &ctx->ev_done})
+        for (cudaEvent_t* ev : {&ctx->ev_ready, &ctx->ev_kv, &ctx->ev_in, &ctx->ev_comp, &ctx->ev_done})
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
                 return cuda_fail(e, "cudaEventCreate");
     }
@@ -508,20 +513,24 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
         const int hc = h0 + chunk <= H ? chunk : H - h0;
         const size_t off = h0 * head_elems * 2, bytes = hc * head_elems * 2;
         const size_t doff = h0 * static_cast<size_t>(n_tokens) * 4, dbytes = hc * static_cast<size_t>(n_tokens) * 4;
+        // K and V first: the chunk's KV kernels wait only for them, the apply also for Q and
+        // the denominators, which are copied while the KV kernels run.
         if ((e = cudaMemcpyAsync(dptr(ctx->st_k, off), hptr(k_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
                 cudaSuccess ||
             (e = cudaMemcpyAsync(dptr(ctx->st_v, off), hptr(v, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
-                cudaSuccess ||
-            (e = cudaMemcpyAsync(dptr(ctx->st_q, off), hptr(q_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+        if ((e = cudaEventRecord(ctx->ev_kv, ctx->s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, ctx->ev_kv, 0)) != cudaSuccess)
+            return cuda_fail(e, "stream ordering");
+        if ((e = cudaMemcpyAsync(dptr(ctx->st_q, off), hptr(q_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
                 cudaSuccess ||
             (e = cudaMemcpyAsync(dptr(ctx->st_den, doff), hptr(normalizer, doff), dbytes, cudaMemcpyHostToDevice,
                                  ctx->s_in)) != cudaSuccess)
             return cuda_fail(e, "host-to-device copy");
-        if ((e = cudaEventRecord(ctx->ev_in, ctx->s_in)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(s, ctx->ev_in, 0)) != cudaSuccess)
-            return cuda_fail(e, "stream ordering");
+        if ((e = cudaEventRecord(ctx->ev_in, ctx->s_in)) != cudaSuccess) return cuda_fail(e, "stream ordering");
         rc = enqueue_heads(ctx, ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_den, ctx->st_out, out_dtype, n_tokens, mode,
-                           s, h0, hc, nullptr);
+                           s, h0, hc, nullptr, LIN_ATTN_LAYOUT_HND, nullptr, nullptr, ctx->ev_in);
         if (rc) return rc;
         if ((e = cudaEventRecord(ctx->ev_comp, s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_comp, 0)) != cudaSuccess)

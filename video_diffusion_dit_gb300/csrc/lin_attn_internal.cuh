@@ -245,9 +245,12 @@ int record_error(int code, const char* msg);
 // Launch `kernel` with programmatic stream serialisation: it may start while the previous
 // kernel of the stream finishes.  Every kernel launched this way calls grid_dependency_wait
 // before it touches memory an earlier kernel of the stream may still be using.
+// With overlap = false the launch is an ordinary one: it starts only after everything
+// before it in the stream (used where an event wait sits between two kernels and the second
+// one reads what the waited-for work produced before its grid-dependency wait).
 template <typename... Params, typename... Args>
-cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                              Args&&... args) {
+cudaError_t launch_kernel(bool overlap, void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -257,8 +260,13 @@ cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = overlap ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+template <typename... Params, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    return launch_kernel(true, kernel, grid, block, smem, stream, static_cast<Args&&>(args)...);
 }
 
 // The producer step fused into the tensor-core kernels (ReLU + interleaved RoPE on the
@@ -340,9 +348,11 @@ cudaError_t launch_kv_finalize(const float* partial, float* kv, uint8_t* kv_imag
                                const KvPlan& plan, cudaStream_t stream, const ProducerArgs* producer = nullptr);
 
 // out = (Q . KV) * (1 / den) on tensor cores, KV as three BF16 terms (maps as above).
+// overlap = false: an ordinary launch (see launch_kernel).
 cudaError_t launch_apply_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_out, const uint8_t* kv_image,
                             const float* den, int heads, int64_t n_tokens, int head_dim, bool out_bf16,
-                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream);
+                            bool token_major, int grid, int* status, uint64_t wait_ns, cudaStream_t stream,
+                            bool overlap = true);
 
 // Softmax anchor attention (flash forward): out = softmax(scale * Q K^T) V per head, no
 // mask.  Maps over [H][N][D] BF16: Q box (64, 128), K and V boxes (64, 64); scale_log2 =
