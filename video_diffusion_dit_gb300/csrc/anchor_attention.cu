@@ -176,21 +176,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             auto wait_full = [&](uint32_t i) {
                 return mbar_wait(kv_full0 + 8u * (i % kSlots), (i / kSlots) & 1u, abort_flag, status, wait_ns);
             };
+            // Descriptors are built once per tile and advanced by the K-step's offset (the
+            // start-address field is bits 0..13 of the descriptor, address >> 4, and no shared
+            // address here carries out of it): the issuing thread, not the tensor pipe, had
+            // been the limit with a descriptor built per instruction.
+            const uint64_t q_desc[kQTiles] = {make_smem_desc(base, 16u, 1024u, kSwizzle128B),
+                                              make_smem_desc(base + L::tile_bytes, 16u, 1024u, kSwizzle128B)};
             auto issue_s = [&](int t, uint32_t kslot) {
-                const uint32_t qa = base + t * L::tile_bytes;
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint32_t off = (ks >> 2) * kAtom + (ks & 3) * 32u;
-                    mma_bf16(tmem + 128u * t, make_smem_desc(qa + off, 16u, 1024u, kSwizzle128B),
-                             make_smem_desc(kslot + off, 16u, 1024u, kSwizzle128B), idesc_s, ks != 0 ? 1u : 0u);
+                const uint64_t kd = make_smem_desc(kslot, 16u, 1024u, kSwizzle128B);
+#pragma unroll
+                for (int ks = 0; ks < 4 * NBOX; ++ks) {
+                    if (ks < ksteps) {
+                        const uint64_t off = ((ks >> 2) * kAtom + (ks & 3) * 32u) >> 4;
+                        mma_bf16(tmem + 128u * t, q_desc[t] + off, kd + off, idesc_s, ks != 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(s_full0 + 8u * t);
             };
             auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+                const uint64_t vd = make_smem_desc(vslot, kAtom, 1024u, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_bf16_ts(tmem + kOCol + 128u * t, tmem + 128u * t + kPCol + 8u * kk,
-                                make_smem_desc(vslot + kk * 2048u, kAtom, 1024u, kSwizzle128B), idesc_o,
-                                (accumulate || kk != 0) ? 1u : 0u);
+                    mma_bf16_ts(tmem + kOCol + 128u * t, tmem + 128u * t + kPCol + 8u * kk, vd + kk * (2048u >> 4),
+                                idesc_o, (accumulate || kk != 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(q_full, 0, abort_flag, status, wait_ns) && wait_full(0);
             if (ok) {
