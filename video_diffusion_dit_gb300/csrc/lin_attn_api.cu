@@ -102,10 +102,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // token-major tile is rows of D elements (224 bytes at D = 112) between other heads' rows,
 // where 256-byte granules fetch the neighbours' bytes too, and they are mostly evicted again
 // before the neighbour's CTA asks for them (22 % extra DRAM reads measured), so 64-byte
-// granules.
+// granules for K and V; the apply's Q (and output) maps take 128-byte granules, which
+// measured faster there (token-major apply 0.3916 -> 0.3787 ms at 720p, while K and V at
+// 128 bytes made the KV kernel slower: 0.3062 -> 0.3152).
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t d, int64_t n,
              int64_t h, uint32_t box_x, uint32_t box_y, bool token_major = false, int64_t heads_total = 0,
-             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+             CUtensorMapL2promotion token_major_promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_64B) {
     auto fn = encode_fn();
     if (!fn) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(h)};
@@ -121,7 +124,7 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_
     }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle, token_major ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, token_major ? token_major_promotion : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LIN_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return LIN_ATTN_OK;
@@ -234,19 +237,22 @@ int enqueue_heads(lin_attn_ctx* c, const void* q, const void* k, const void* v, 
         return cuda_fail(e, "stream ordering");
     {
         CUtensorMap tq, to;
-        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H);
+        int rc = make_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, la::kApplyTile, tm, H,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
         if (rc) return rc;
         if (fused) {  // transposed epilogue: (32 features, 32 tokens) boxes, unswizzled
             rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 32, 32, tm, H,
-                                     CU_TENSOR_MAP_SWIZZLE_NONE)
+                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)
                           : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H,
-                                     CU_TENSOR_MAP_SWIZZLE_NONE);
+                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
             if (rc) return rc;
             e = la::launch_apply_fused_tc(tq, to, image_h0, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, c->wait_ns,
                                           stream, pa_apply);
         } else {
-            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H)
-                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H);
+            rc = bf16_out ? make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, n_tokens, hc, 64, 32, tm, H,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)
+                          : make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, n_tokens, hc, 32, 32, tm, H,
+                                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
             if (rc) return rc;
             e = la::launch_apply_tc(tq, to, image_h0, den, hc, n_tokens, D, bf16_out, tm, c->n_sms, c->status, c->wait_ns,
                                     stream, apply_after == nullptr);
