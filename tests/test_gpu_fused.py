@@ -88,11 +88,12 @@ def test_fused_480p(la, dev):
     check(la, dev, w.heads, w.tokens, w.head_dim, w.seed, w.grid, dtypes=(torch.float32,))
 
 
-def test_fused_720p_whole_tensor(la, dev):
-    """The full 720p layer through the fused call, every output element against the oracle,
-    both tiers and output types; the model's token-major layout gives the same bits; repeated
-    calls are bitwise identical."""
-    w = synth.WORKLOADS["720p_193f"]
+@pytest.mark.parametrize("name", ["720p_193f", "720p_193f_d64"])
+def test_fused_720p_whole_tensor(la, dev, name):
+    """The full 720p layer (and its D=64, H=32 shape) through the fused call, every output
+    element against the oracle, both tiers and output types; the model's token-major layout
+    gives the same bits; repeated calls are bitwise identical."""
+    w = synth.WORKLOADS[name]
     H, N, D = w.heads, w.tokens, w.head_dim
     layer = synth.make_workload(w, device=dev, producer_inputs=True)
     ref, kv_ref = oracle_fused(layer)
@@ -105,7 +106,7 @@ def test_fused_720p_whole_tensor(la, dev):
                 out = ctx.forward_fused(layer["q"], layer["k"], layer["v"], *tabs, out_dtype=dt, mode=mode)
                 assert ctx.device_status() == 0
                 whole, head = whole_and_head_rel_l2(out, ref)
-                assert whole <= TOL[dt] and head <= TOL[dt], f"fused 720p {mode} {dt}: {whole:.3e} / {head:.3e}"
+                assert whole <= TOL[dt] and head <= TOL[dt], f"fused {name} {mode} {dt}: {whole:.3e} / {head:.3e}"
                 assert rel_l2(ctx.debug_kv().double().cpu().numpy(), kv_ref) <= 1e-6
                 tm = ctx.forward_fused(nhd["q"], nhd["k"], nhd["v"], *tabs, out_dtype=dt, mode=mode, layout="nhd")
                 assert ctx.device_status() == 0
