@@ -17,18 +17,19 @@ namespace la {
 namespace {
 
 // ============================================================================ tensor cores
-// Persistent: each CTA owns a contiguous range of 128-token tiles in (head, tile) order.
-// Warp 0 streams Q tiles with TMA (two 64-column boxes, 128-byte swizzle = K-major MMA
-// layout) and, when the head changes, bulk-copies that head's KV image (three BF16 terms
-// KV = hi + mid + lo, already in the swizzled K-major B layout) into shared memory.
-// Warp 1 issues, per tile, 3 terms x (Dpad / 16) MMAs of 128 x D x 16 into one of two TMEM
-// accumulators.  Warps 2..9 read the accumulator (one token row per thread; two warps per
-// TMEM lane quarter, each with half of the tile's column groups), multiply by the
-// reciprocal denominator and write 32-row boxes through swizzled staging with TMA stores:
-// two staging buffers per warp when the head dim fits one 64-column atom, one otherwise
-// (the 86 KB KV image leaves room for no more).  BF16 x BF16 products are exact in FP32 and
-// the three terms carry 24 bits of KV, so the result has FP32-class accuracy (the tier's
-// second GEMM "stays FP32").
+// Persistent: each CTA owns a contiguous range of 128-token tiles in (head, tile) order
+// (token-major activations: a chunk of the body + tail split).  Warp 0 streams Q tiles with
+// TMA (two 64-column boxes, 128-byte swizzle = K-major MMA layout) and, when the head
+// changes, bulk-copies that head's KV image (three BF16 terms KV = hi + mid + lo, already in
+// the swizzled K-major B layout) into shared memory.  Warp 1 issues, per tile, 3 terms x
+// (Dpad / 16) MMAs of 128 x D x 16 into one of the TMEM accumulators (two, or four when
+// D <= 64).  Warps 2..9 read the accumulator (one token row per thread; two warps per TMEM
+// lane quarter, each with half of the tile's column groups, or alternate tiles where there
+// is one group), multiply by the reciprocal denominator (loaded a tile ahead) and write
+// 32-row boxes through swizzled staging with TMA stores (stage and staging-buffer counts in
+// apply_stages / apply_out_bufs).  BF16 x BF16 products are exact in FP32 and the three
+// terms carry 24 bits of KV, so the result has FP32-class accuracy (the tier's second GEMM
+// "stays FP32").
 constexpr int kApplyEpiWarps = 8;
 constexpr int kApplyThreads = 32 * (2 + kApplyEpiWarps);
 constexpr uint32_t kQAtomBytes = kApplyTile * 128;  // 128 token rows x 128 bytes
