@@ -83,6 +83,19 @@ def test_two_calls_in_a_row_match_the_context_path(la, dev, mode, dt):
         assert err <= TOL[dt], f"{mode} {dt} {tuple(g['q_rot'].shape)}: rel-L2 {err:.3e} against the oracle"
 
 
+def test_shared_tail_plan_matches_the_context_path(la, dev):
+    """A length where the spare CTAs share the tails of all heads (9 partial slots per head):
+    the scratch is carved for that many slots and the result is the context call's bits."""
+    H, N, D = 20, 120000, 112
+    assert la.kv_plan(H, N) == (152, 9)
+    g = synth.make_layer(H, N, D, seed=23, device=dev)
+    for mode in ("high", "lossless"):
+        got = noalloc_call(la, g, mode, torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(got, context_call(la, g, mode, torch.float32, dev)), mode
+        assert la.noalloc_status(dev) == la.OK
+
+
 def test_scratch_limit_boundary(la, dev):
     """At head dim 128 with one partial slot per head the 48 MiB array holds 219 heads: 219 is
     accepted (and gives the context call's bits), 220 is refused before any launch."""
