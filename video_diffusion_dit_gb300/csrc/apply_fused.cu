@@ -21,10 +21,11 @@
 //   warp 1      3 terms x D/16 K-steps of tcgen05.mma M=128 (features) N=128 (tokens) into
 //               one of two TMEM accumulators;
 //   warps 2..9  epilogue, a thread per output feature (two warps per TMEM lane quarter,
-//               each with two of a tile's four 32-token chunks): on a head change they
-//               copy the head's image rows into TMEM; per chunk they scale by the tokens'
-//               reciprocal denominators and write [token][feature] boxes to staging for
-//               TMA stores;
+//               each with two of a tile's four 32-token chunks; at D <= 64 the features sit
+//               in both halves of the lanes and each warp takes one chunk): on a head change
+//               they copy the head's image rows into TMEM; per chunk they scale by the
+//               tokens' reciprocal denominators and write [token][feature] boxes to staging
+//               for TMA stores;
 //   warps 10..25 producer step: ReLU + rotation of the Q tile in place, the row
 //               normaliser, its correctly rounded reciprocal to the epilogue.
 // The two warp groups that do per-element work are wide (8 and 16 warps) because each
@@ -352,12 +353,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mbar_arrive(den_full0 + 8u * db);
         }
     } else {
-        // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes = output features
-        // 32q..32q+31, thread = feature j; half e takes token chunks 2e, 2e + 1 of each tile.
+        // ---------------- epilogue: warp (q = warp % 4) owns TMEM lanes 32q..32q+31, thread =
+        // output feature j.  When the head dim spans two atoms, lane = feature and half e takes
+        // token chunks 2e, 2e + 1 of each tile.  When it fits one (D <= 64), lanes 64..127 hold
+        // a second copy of features 0..63 (the image rows are written twice, so the product
+        // computes them twice at no cost: M is 128 either way), and each of the eight warps
+        // takes one chunk of one feature half - chunk 2e + q / 2, features 32 (q % 2) ... - so
+        // that no warp sits idle on the empty upper lanes.
         const int q = warp & 3;
         const int e = (warp - 2) >> 2;
-        const int j = 32 * q + lane;
-        const bool live = 32 * q < head_dim;  // any of the warp's features exists
+        const int j = NBOX == 1 ? 32 * (q & 1) + lane : 32 * q + lane;  // output feature
+        const int fq = NBOX == 1 ? (q & 1) : q;                          // its 32-feature block
+        const bool live = 32 * fq < head_dim;  // any of the warp's features exists
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t stage0 = o_smem + static_cast<uint32_t>(warp - 2) * kFOutBufs * kFBoxBytes;
         // Token-major output rows share L2 lines with the neighbouring heads' rows (written by
@@ -414,7 +421,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (!(ok = mbar_wait(acc_full0 + 8u * buf, (lt >> 1) & 1u, abort_flag, status, wait_ns))) break;
             tc_fence_after();
             const float* rcp_t = rcp_s + db * kApplyTile;
-            for (int g = 2 * e; g < 2 * e + 2 && n0 + 32 * g < n_tokens; ++g) {
+            const int g0 = NBOX == 1 ? 2 * e + (q >> 1) : 2 * e, g1 = NBOX == 1 ? g0 + 1 : g0 + 2;
+            for (int g = g0; g < g1 && n0 + 32 * g < n_tokens; ++g) {
                 uint32_t r[32];
                 tmem_ld32_sync(tmem + lane_base + buf * kFAccCols + 32u * g, r);
                 if (!live) continue;
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d_hint(&tm_out, sbuf, 32 * q, token_major ? h : n0 + 32 * g,
+                    tma_store_3d_hint(&tm_out, sbuf, 32 * fq, token_major ? h : n0 + 32 * g,
                                       token_major ? n0 + 32 * g : h, spol);
                     bulk_commit();
                 }
