@@ -48,11 +48,12 @@ template <int NBOX, bool FUSED>
 struct KvLayout {
     // The fused path also stages the tile's rows of the two rotation tables (FP32,
     // [64 tokens][D/2], at most 16 KB each) in a ring of their own: the tables mostly come
-    // from L2 (every head reads the same rows), K and V from DRAM, so the K/V ring keeps
-    // four tiles in flight and the table ring three (a table copy is issued two tiles
-    // before its transform).
+    // from L2 (every head reads the same rows), K and V from DRAM.  When D > 64 the K/V ring
+    // keeps four tiles in flight and the table ring three (a table copy is issued two tiles
+    // before its transform); when D <= 64 six and four, since a tile then takes about half
+    // the time and the table ring must still cover a copy's ~1.8 us from L2.
     static constexpr int stages = FUSED ? (NBOX == 1 ? 6 : 4) : kKvStages;
-    static constexpr int tab_ring = 3;                  // table slots of the fused kernel
+    static constexpr int tab_ring = NBOX == 1 ? 4 : 3;  // table slots of the fused kernel
     static constexpr int tab_slots = FUSED ? tab_ring : 0;  // ... and the shared memory they take
     static constexpr uint32_t a_bytes = 2 * kKvAtomBytes;  // A = K^T: 2 atoms cover M = 128
     static constexpr uint32_t b_bytes = NBOX * kKvAtomBytes;
@@ -60,7 +61,8 @@ struct KvLayout {
     static constexpr uint32_t stage_bytes = a_bytes + b_bytes;
     static constexpr uint32_t tab_offset = stages * stage_bytes;  // [tab_slots][cos, sin]
     static constexpr uint32_t bar_offset = tab_offset + tab_slots * 2 * tab_bytes;
-    static constexpr uint32_t smem_bytes = bar_offset + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t bar_bytes = 512;
+    static constexpr uint32_t smem_bytes = bar_offset + bar_bytes + 1024;  // + barriers + alignment slack
     // TMEM: two 128-column accumulators; the fused kernel keeps the segment's running sum in
     // a third region (columns 256..383) instead of registers, which leaves the registers to
     // its transform warps.
@@ -112,9 +114,10 @@ __global__ void __launch_bounds__(FUSED ? kKvThreadsFused : kKvThreads, 1)
     const uint32_t ready0 = drain_bar + 8u;               // [L::stages] (fused: tile transformed)
     const uint32_t tab_full0 = ready0 + 8u * L::stages;   // [L::tab_slots] (fused: table rows landed)
     const uint32_t tab_empty0 = tab_full0 + 8u * L::tab_slots;  // [L::tab_slots] (... and used)
-    static_assert(3 * L::stages * 8 + 40 + 16 * L::tab_slots <= 240, "barriers overlap the TMEM address slot");
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + 240);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + 248);
+    static_assert(3 * L::stages * 8 + 40 + 16 * L::tab_slots <= L::bar_bytes - 16,
+                  "barriers overlap the TMEM address slot");
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + L::bar_offset + L::bar_bytes - 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::bar_offset + L::bar_bytes - 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
