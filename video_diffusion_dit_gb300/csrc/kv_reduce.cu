@@ -68,6 +68,7 @@ struct KvLayout {
     // its transform warps.
     static constexpr uint32_t tmem_cols = FUSED ? 512 : 256;
     static constexpr uint32_t sum_col = 256;
+    static_assert(!FUSED || sum_col + 128 <= tmem_cols, "the running sums must fit beside the accumulators");
 };
 
 static_assert(KvLayout<2, true>::smem_bytes <= 232448 && KvLayout<2, false>::smem_bytes <= 232448 &&
