@@ -385,7 +385,9 @@ def run_ours(args, w, world, rank, local, dist):
     host = {k: t.cpu().pin_memory() for k, t in layer.items()}
     hout = torch.empty(1, H, N, D, dtype=out_dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode, stream=stream)
+    for _ in range(2):  # untimed: the first calls also touch the pinned pages and the staging buffers
+        ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
+                         stream=stream)
     barrier(dist, dev)
     t0 = time.perf_counter()
     e2e_step_ms = []
@@ -618,7 +620,7 @@ def main():
     ap.add_argument("--workload", default="720p_193f")
     ap.add_argument("--mode", default="high", choices=["high", "lossless"])
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "bf16"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--layers", type=int, default=2,
                     help="distinct seeded layers visited in turn, one per step (2: no step finds the previous "
                          "step's data in L2)")
