@@ -6,8 +6,10 @@ N=180320, D=112, 'high' tier, FP32 output) unless --workload/--mode say otherwis
 
 Prints ONE JSON line (rank 0):
   value      tokens/s per layer call, inputs resident in HBM (device-timed, CUDA events)
-  e2e        the same metric through the C ABI's host-buffer call (pinned host memory;
-             host->device copies of q/k/v/den and the device->host copy of out are inside)
+  e2e        the same metric with the inputs starting in pinned host memory and the output
+             ending there (copies inside the timed region): the head-major call through the
+             C ABI's host-buffer call; the fused and token-major calls, which have no
+             host-buffer form, as copies in + the call + copy out (`e2e.api` says which)
   roofline   the dominant kernel's algorithmic bytes / its mean event-timed duration
              against the measured HBM copy bandwidth
   cpu_baseline  the FP64 oracle on the host cores on a bounded sample of the same layer
@@ -378,26 +380,51 @@ def run_ours(args, w, world, rank, local, dist):
                 for j, name in enumerate(("kv_partial", "kv_finalize", "apply"))}
     call_ms = call_percentiles(step, min(args.steps, 500), stream, dev)
 
-    # ---- end to end through the host-buffer entry point (pinned host memory, [1, H, N, D])
-    if args.layout == "nhd":
-        layer = {k: (t.permute(0, 2, 1, 3).contiguous() if t.dim() == 4 and k != "den" else t)
-                 for k, t in layer.items()}
-    host = {k: t.cpu().pin_memory() for k, t in layer.items()}
-    hout = torch.empty(1, H, N, D, dtype=out_dtype).pin_memory()
+    # ---- end to end from pinned host memory and back.  The head-major call goes through the
+    # host-buffer entry point, which pipelines its copies with the kernels.  The calls that
+    # have no host-buffer form (fused producer, token-major activations) copy their inputs
+    # in, run the timed call on the device copies and copy the output back.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hout = torch.empty(tuple(out.shape), dtype=out_dtype).pin_memory()
+    if args.fused or args.layout == "nhd":
+        keys = ("q", "k", "v", "rope_cos", "rope_sin") if args.fused else ("q_rot", "k_rot", "v", "den")
+        host = {k: layer[k].cpu().pin_memory() for k in keys}
+        dbuf = {k: torch.empty_like(layer[k]) for k in keys}
+        e2e_api = "copies in + " + ("lin_attn_forward_fused" if args.fused else "lin_attn_forward_layout") + \
+                  " + copy out"
+
+        def e2e_call():
+            for k in keys:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            if args.fused:
+                ctx.forward_fused(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["rope_cos"], dbuf["rope_sin"], out=out,
+                                  stream=stream, layout=args.layout, mode=args.mode)
+            else:
+                ctx.forward(dbuf["q_rot"], dbuf["k_rot"], dbuf["v"], dbuf["den"], out=out, mode=args.mode,
+                            stream=stream, layout=args.layout)
+            hout.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    else:
+        host = {k: layer[k].cpu().pin_memory() for k in ("q_rot", "k_rot", "v", "den")}
+        e2e_api = "lin_attn_forward_host"
+
+        def e2e_call():
+            ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
+                             stream=stream)
+
+        h2d = 3 * H * N * D * 2 + H * N * 4
     for _ in range(2):  # untimed: the first calls also touch the pinned pages and the staging buffers
-        ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
-                         stream=stream)
+        e2e_call()
     barrier(dist, dev)
     t0 = time.perf_counter()
     e2e_step_ms = []
     for _ in range(e2e_steps):
         t1 = time.perf_counter()
-        ctx.forward_host(host["q_rot"], host["k_rot"], host["v"], host["den"], out=hout, mode=args.mode,
-                         stream=stream)
+        e2e_call()
         e2e_step_ms.append((time.perf_counter() - t1) * 1e3)
     e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev) / e2e_steps
-    h2d = 3 * H * N * D * 2 + H * N * 4
     d2h = H * N * D * out_bytes
 
     nbytes = algorithmic_bytes(H, N, D, out_bytes)
@@ -438,6 +465,7 @@ def run_ours(args, w, world, rank, local, dist):
             "e2e": {"value": world * N / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "step_ms": {"min": min(e2e_step_ms), "p50": float(np.median(e2e_step_ms)), "max": max(e2e_step_ms)},
+                    "api": e2e_api,
                     "note": "bound by the host-device link; varies with other traffic on the host"},
             "gpu_launches": 3 * args.steps,
             "stage_ms_note": "per-kernel means from a second pass of the same steps with events around each kernel",
