@@ -1,6 +1,7 @@
-"""The layer calls put only stream work on the caller's stream (kernel launches with
-programmatic dependencies, no host synchronisation, no allocation), so a sequence of them
-can be captured into a CUDA graph: replayed, the graph gives the eager calls' bits."""
+"""Stream behaviour of the layer calls.  They put only stream work on the caller's stream
+(kernel launches with programmatic dependencies, no host synchronisation, no allocation),
+so a sequence of them can be captured into a CUDA graph: replayed, the graph gives the
+eager calls' bits.  Contexts share no device state, so two of them may run at once."""
 import pytest
 import torch
 
@@ -55,4 +56,25 @@ def test_layer_calls_replay_from_a_cuda_graph(la, dev):
         torch.cuda.synchronize()
         assert ctx.device_status() == la.OK
         for o, w in zip(got, want):
+            assert torch.equal(o, w)
+
+
+def test_two_contexts_on_two_streams_at_once(la, dev):
+    """Each context owns its scratch: two contexts running on two streams at the same time
+    give the bits each gives alone."""
+    H, N, D = 6, 30000, 112
+    layers = [{k: t.to(dev) for k, t in synth.make_layer(H, N, D, seed).items()} for seed in (41, 42)]
+    with la.LinAttn(H, N, D, dev) as a, la.LinAttn(H, N, D, dev) as b:
+        alone = []
+        for ctx, g in zip((a, b), layers):
+            alone.append(ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"]).clone())
+        torch.cuda.synchronize()
+        streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        outs = [torch.zeros(1, H, N, D, device=dev) for _ in range(2)]
+        for _ in range(3):
+            for ctx, g, s, o in zip((a, b), layers, streams, outs):
+                ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], out=o, stream=s)
+        torch.cuda.synchronize()
+        assert a.device_status() == la.OK and b.device_status() == la.OK
+        for o, w in zip(outs, alone):
             assert torch.equal(o, w)
