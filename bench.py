@@ -7,9 +7,9 @@ N=180320, D=112, 'high' tier, FP32 output) unless --workload/--mode say otherwis
 Prints ONE JSON line (rank 0):
   value      tokens/s per layer call, inputs resident in HBM (device-timed, CUDA events)
   e2e        the same metric with the inputs starting in pinned host memory and the output
-             ending there (copies inside the timed region): the head-major call through the
-             C ABI's host-buffer call; the fused and token-major calls, which have no
-             host-buffer form, as copies in + the call + copy out (`e2e.api` says which)
+             ending there (copies inside the timed region): the head-major calls through the
+             C ABI's host-buffer calls; the token-major calls, which have no host-buffer
+             form, as copies in + the call + copy out (`e2e.api` says which)
   roofline   the dominant kernel's algorithmic bytes / its mean event-timed duration
              against the measured HBM copy bandwidth
   cpu_baseline  the FP64 oracle on the host cores on a bounded sample of the same layer
@@ -380,13 +380,23 @@ def run_ours(args, w, world, rank, local, dist):
                 for j, name in enumerate(("kv_partial", "kv_finalize", "apply"))}
     call_ms = call_percentiles(step, min(args.steps, 500), stream, dev)
 
-    # ---- end to end from pinned host memory and back.  The head-major call goes through the
-    # host-buffer entry point, which pipelines its copies with the kernels.  The calls that
-    # have no host-buffer form (fused producer, token-major activations) copy their inputs
-    # in, run the timed call on the device copies and copy the output back.
+    # ---- end to end from pinned host memory and back.  The head-major calls go through their
+    # host-buffer entry points, which pipeline the copies with the kernels.  The token-major
+    # calls, which have no host-buffer form, copy their inputs in, run the timed call on the
+    # device copies and copy the output back.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     hout = torch.empty(tuple(out.shape), dtype=out_dtype).pin_memory()
-    if args.fused or args.layout == "nhd":
+    if args.fused and args.layout == "hnd":
+        keys = ("q", "k", "v", "rope_cos", "rope_sin")
+        host = {k: layer[k].cpu().pin_memory() for k in keys}
+        e2e_api = "lin_attn_forward_fused_host"
+
+        def e2e_call():
+            ctx.forward_fused_host(host["q"], host["k"], host["v"], host["rope_cos"], host["rope_sin"], out=hout,
+                                   mode=args.mode, stream=stream)
+
+        h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    elif args.layout == "nhd":
         keys = ("q", "k", "v", "rope_cos", "rope_sin") if args.fused else ("q_rot", "k_rot", "v", "den")
         host = {k: layer[k].cpu().pin_memory() for k in keys}
         dbuf = {k: torch.empty_like(layer[k]) for k in keys}

@@ -177,6 +177,20 @@ int lin_attn_forward_host(lin_attn_ctx *ctx, const void *q_rot, const void *k_ro
                           int mode, struct CUstream_st *stream);
 
 /*
+ * The fused-producer layer call (lin_attn_forward_fused, head-major) on HOST buffers:
+ * q, k, v BF16 [1, heads, n_tokens, head_dim], rope_cos / rope_sin FP32
+ * [n_tokens, head_dim / 2], out FP32 or BF16 [1, heads, n_tokens, head_dim], any
+ * alignment.  The same pipeline as lin_attn_forward_host (and its staging, streams and
+ * events), with the two tables copied once ahead of the first chunk (their staging,
+ * 2 x max_tokens x head_dim / 2 FP32, is allocated on the first call: LIN_ATTN_ERR_OOM if
+ * it cannot be); synchronises `stream` before returning, and the result is bitwise the
+ * one lin_attn_forward_fused gives.  NULL tables: LIN_ATTN_ERR_INVALID_ARG.
+ */
+int lin_attn_forward_fused_host(lin_attn_ctx *ctx, const void *q, const void *k, const void *v,
+                                const float *rope_cos, const float *rope_sin, void *out, int out_dtype,
+                                int64_t n_tokens, int mode, struct CUstream_st *stream);
+
+/*
  * Test hook: enqueue a copy of the reduced KV of the last forward call, FP32
  * [heads, head_dim, head_dim] row-major (KV[h][i][j] = sum_n K_rot[h][n][i] V[h][n][j]),
  * into the device buffer kv_out.

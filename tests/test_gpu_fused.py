@@ -155,3 +155,27 @@ def test_fused_lossless(la, dev, shape):
         assert rel_l2(kv_fused.double().cpu().numpy(), kv_ref) <= 1e-6
         ctx.forward(g["q_rot"], g["k_rot"], g["v"], g["den"], mode="lossless")
         assert torch.equal(ctx.debug_kv(), kv_fused)
+
+
+@pytest.mark.parametrize("shape", [(5, 3001, 112), (3, 777, 64), (20, 120000, 112)])
+def test_fused_host_buffers_are_bitwise_the_device_call(la, dev, shape):
+    # The host-buffer form pipelines the copies over chunks of heads; every chunk runs the
+    # layer's own split, so its result is the device call's bits.  (20, 120000): the spare
+    # CTAs share the tails of all heads, so the chunks' launches reproduce shared segments.
+    H, N, D = shape
+    layer = synth.make_layer(H, N, D, 11 * N + H, producer_inputs=True)
+    keys = ("q", "k", "v", "rope_cos", "rope_sin")
+    host = {key: layer[key].contiguous().pin_memory() for key in keys}
+    g = {key: layer[key].to(dev) for key in keys}
+    with la.LinAttn(H, N, D, dev) as ctx:
+        for mode in ("high", "lossless"):
+            for dt in (torch.float32, torch.bfloat16):
+                want = ctx.forward_fused(g["q"], g["k"], g["v"], g["rope_cos"], g["rope_sin"], out_dtype=dt,
+                                         mode=mode).cpu()
+                got = ctx.forward_fused_host(host["q"], host["k"], host["v"], host["rope_cos"], host["rope_sin"],
+                                             out_dtype=dt, mode=mode)
+                assert ctx.device_status() == 0
+                assert torch.equal(got, want), (mode, dt)
+        bad = [host["q"].data_ptr(), host["k"].data_ptr(), host["v"].data_ptr(), 0, host["rope_sin"].data_ptr(),
+               got.data_ptr(), la.OUT_BF16, N, la.MODE_HIGH, torch.cuda.current_stream().cuda_stream]
+        assert la.lib.lin_attn_forward_fused_host(ctx._h, *bad) == la.ERR_INVALID_ARG

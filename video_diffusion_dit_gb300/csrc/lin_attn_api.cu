@@ -32,6 +32,8 @@ struct lin_attn_ctx {
     void* st_v = nullptr;
     float* st_den = nullptr;
     void* st_out = nullptr;
+    float* st_cos = nullptr;  // fused host-buffer path: the rotation tables [max_tokens][D/2]
+    float* st_sin = nullptr;
     // host-buffer pipeline: copy streams and ordering events, created on first use
     cudaStream_t s_in = nullptr;
     cudaStream_t s_out = nullptr;
@@ -158,6 +160,8 @@ void free_all(lin_attn_ctx* c) {
     cudaFree(c->st_v);
     cudaFree(c->st_den);
     cudaFree(c->st_out);
+    cudaFree(c->st_cos);
+    cudaFree(c->st_sin);
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
     for (cudaEvent_t ev : {c->ev_ready, c->ev_kv, c->ev_in, c->ev_comp, c->ev_done})
@@ -467,13 +471,17 @@ int lin_attn_anchor_forward(lin_attn_ctx* ctx, const void* q, const void* k, con
     return ok();
 }
 
-int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,
-                          const float* normalizer, void* out, int out_dtype, int64_t n_tokens, int mode,
-                          struct CUstream_st* stream) {
-    int rc = check_call(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode);
-    if (rc) return rc;
+namespace {
+
+// The host-buffer pipeline shared by the plain and the fused call.  den is the plain call's
+// denominators; rope_cos / rope_sin (both or neither) make it the fused call, whose tables
+// are copied once, ahead of the first chunk's K and V.
+int host_pipeline(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* den,
+                  const float* rope_cos, const float* rope_sin, void* out, int out_dtype, int64_t n_tokens, int mode,
+                  cudaStream_t s) {
     DeviceScope scope(ctx->device);
     if (scope.err != cudaSuccess) return cuda_fail(scope.err, "cudaSetDevice");
+    const bool fused = rope_cos != nullptr;
     const size_t elems_max = static_cast<size_t>(ctx->heads) * ctx->max_tokens * ctx->head_dim;
     if (!ctx->st_q) {
         bool good = cudaMalloc(&ctx->st_q, 2 * elems_max) == cudaSuccess &&
@@ -493,6 +501,17 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
             return fail(LIN_ATTN_ERR_OOM, "device allocation of the host-path staging failed");
         }
     }
+    const size_t table_bytes = static_cast<size_t>(n_tokens) * (ctx->head_dim / 2) * sizeof(float);
+    if (fused && !ctx->st_cos) {
+        const size_t max_bytes = static_cast<size_t>(ctx->max_tokens) * (ctx->head_dim / 2) * sizeof(float);
+        if (cudaMalloc(&ctx->st_cos, max_bytes) != cudaSuccess || cudaMalloc(&ctx->st_sin, max_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(ctx->st_cos);
+            cudaFree(ctx->st_sin);
+            ctx->st_cos = ctx->st_sin = nullptr;
+            return fail(LIN_ATTN_ERR_OOM, "device allocation of the host-path table staging failed");
+        }
+    }
     cudaError_t e;
     if (!ctx->s_in) {
         if ((e = cudaStreamCreateWithFlags(&ctx->s_in, cudaStreamNonBlocking)) != cudaSuccess ||
@@ -505,7 +524,6 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
     // Pipeline over chunks of heads: host-to-device copies on one stream, the kernels on
     // the caller's stream, device-to-host copies on a third, so both copy directions and
     // the compute overlap.  Each chunk waits only for its own inputs.
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int H = ctx->heads, chunk = host_chunk_heads(H);
     const size_t head_elems = static_cast<size_t>(n_tokens) * ctx->head_dim;
     const size_t out_es = out_dtype == LIN_ATTN_OUT_BF16 ? 2 : 4;
@@ -515,13 +533,19 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
         (e = cudaStreamWaitEvent(ctx->s_in, ctx->ev_ready, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_ready, 0)) != cudaSuccess)
         return cuda_fail(e, "stream ordering");
+    if (fused && ((e = cudaMemcpyAsync(ctx->st_cos, rope_cos, table_bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                      cudaSuccess ||
+                  (e = cudaMemcpyAsync(ctx->st_sin, rope_sin, table_bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+                      cudaSuccess))
+        return cuda_fail(e, "host-to-device copy");
     for (int h0 = 0; h0 < H; h0 += chunk) {
         const int hc = h0 + chunk <= H ? chunk : H - h0;
         const size_t off = h0 * head_elems * 2, bytes = hc * head_elems * 2;
         const size_t doff = h0 * static_cast<size_t>(n_tokens) * 4, dbytes = hc * static_cast<size_t>(n_tokens) * 4;
-        // K and V first: the chunk's KV kernels wait only for them, the apply also for Q and
-        // the denominators, which are copied while the KV kernels run.
-        if ((e = cudaMemcpyAsync(dptr(ctx->st_k, off), hptr(k_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+        // K and V first (and, on the fused path, the tables before the first chunk): the
+        // chunk's KV kernels wait only for them, the apply also for Q (and the denominators),
+        // which are copied while the KV kernels run.
+        if ((e = cudaMemcpyAsync(dptr(ctx->st_k, off), hptr(k, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
                 cudaSuccess ||
             (e = cudaMemcpyAsync(dptr(ctx->st_v, off), hptr(v, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
                 cudaSuccess)
@@ -529,14 +553,16 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
         if ((e = cudaEventRecord(ctx->ev_kv, ctx->s_in)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(s, ctx->ev_kv, 0)) != cudaSuccess)
             return cuda_fail(e, "stream ordering");
-        if ((e = cudaMemcpyAsync(dptr(ctx->st_q, off), hptr(q_rot, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
-                cudaSuccess ||
-            (e = cudaMemcpyAsync(dptr(ctx->st_den, doff), hptr(normalizer, doff), dbytes, cudaMemcpyHostToDevice,
-                                 ctx->s_in)) != cudaSuccess)
+        if ((e = cudaMemcpyAsync(dptr(ctx->st_q, off), hptr(q, off), bytes, cudaMemcpyHostToDevice, ctx->s_in)) !=
+            cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+        if (!fused && (e = cudaMemcpyAsync(dptr(ctx->st_den, doff), hptr(den, doff), dbytes, cudaMemcpyHostToDevice,
+                                           ctx->s_in)) != cudaSuccess)
             return cuda_fail(e, "host-to-device copy");
         if ((e = cudaEventRecord(ctx->ev_in, ctx->s_in)) != cudaSuccess) return cuda_fail(e, "stream ordering");
-        rc = enqueue_heads(ctx, ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_den, ctx->st_out, out_dtype, n_tokens, mode,
-                           s, h0, hc, nullptr, LIN_ATTN_LAYOUT_HND, nullptr, nullptr, ctx->ev_in);
+        const int rc = enqueue_heads(ctx, ctx->st_q, ctx->st_k, ctx->st_v, fused ? nullptr : ctx->st_den, ctx->st_out,
+                                     out_dtype, n_tokens, mode, s, h0, hc, nullptr, LIN_ATTN_LAYOUT_HND,
+                                     fused ? ctx->st_cos : nullptr, fused ? ctx->st_sin : nullptr, ctx->ev_in);
         if (rc) return rc;
         if ((e = cudaEventRecord(ctx->ev_comp, s)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_comp, 0)) != cudaSuccess)
@@ -551,6 +577,28 @@ int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_ro
         return cuda_fail(e, "stream ordering");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return ok();
+}
+
+}  // namespace
+
+int lin_attn_forward_host(lin_attn_ctx* ctx, const void* q_rot, const void* k_rot, const void* v,
+                          const float* normalizer, void* out, int out_dtype, int64_t n_tokens, int mode,
+                          struct CUstream_st* stream) {
+    const int rc = check_call(ctx, q_rot, k_rot, v, normalizer, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    return host_pipeline(ctx, q_rot, k_rot, v, normalizer, nullptr, nullptr, out, out_dtype, n_tokens, mode,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lin_attn_forward_fused_host(lin_attn_ctx* ctx, const void* q, const void* k, const void* v, const float* rope_cos,
+                                const float* rope_sin, void* out, int out_dtype, int64_t n_tokens, int mode,
+                                struct CUstream_st* stream) {
+    if (!rope_cos || !rope_sin) return fail(LIN_ATTN_ERR_INVALID_ARG, "rotation table pointer is NULL");
+    // check_call wants a denominator pointer; the fused call forms the denominators itself.
+    const int rc = check_call(ctx, q, k, v, rope_cos, out, out_dtype, n_tokens, mode);
+    if (rc) return rc;
+    return host_pipeline(ctx, q, k, v, nullptr, rope_cos, rope_sin, out, out_dtype, n_tokens, mode,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int lin_attn_debug_kv(lin_attn_ctx* ctx, float* kv_out, struct CUstream_st* stream) {

@@ -23,7 +23,7 @@ EXPORTS = (
     "lin_attn_debug_kv", "lin_attn_device_status", "lin_attn_kv_plan",
     "lin_attn_set_stage_events", "lin_attn_error_string", "lin_attn_last_error", "lin_attn_version",
     "lin_attn_forward_noalloc", "lin_attn_forward_fused", "lin_attn_anchor_forward", "lin_attn_forward_fused_layout",
-    "lin_attn_set_wait_limit", "lin_attn_noalloc_status",
+    "lin_attn_set_wait_limit", "lin_attn_noalloc_status", "lin_attn_forward_fused_host",
 )
 
 
@@ -50,6 +50,7 @@ def _load():
         "lin_attn_noalloc_status": ([p], i32),
         "lin_attn_forward_fused": ([p, p, p, p, p, p, p, i32, i64, i32, p], i32),
         "lin_attn_forward_fused_layout": ([p, p, p, p, p, p, p, i32, i64, i32, i32, p], i32),
+        "lin_attn_forward_fused_host": ([p, p, p, p, p, p, p, i32, i64, i32, p], i32),
         "lin_attn_anchor_forward": ([p, p, p, p, p, i32, i64, ctypes.c_float, p], i32),
     }
     for name, (args, res) in sig.items():
@@ -279,6 +280,33 @@ class LinAttn:
                                        normalizer.data_ptr(), out.data_ptr(), _out_code(out.dtype), n, _mode(mode),
                                        _stream_handle(stream, self.device))
         _check(st, "lin_attn_forward_host")
+        return out
+
+    def forward_fused_host(self, q, k, v, rope_cos, rope_sin, out=None, mode="high", out_dtype=torch.float32,
+                           stream=None):
+        """The fused-producer call (head-major) on host tensors (pinned for full copy speed):
+        q, k, v BF16 [1, H, N, D], rope_cos / rope_sin FP32 [N, D/2]; blocks until ``out``
+        is filled."""
+        cpu = torch.device("cpu")
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != cpu:
+                raise ValueError(f"{name} must be a contiguous bfloat16 host tensor")
+        if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.shape[0] != 1:
+            raise ValueError("q, k, v must share one 4-D shape with batch 1")
+        _, H, N, D = q.shape
+        if H != self.heads or D != self.head_dim:
+            raise ValueError(f"context is for H={self.heads}, D={self.head_dim}; got H={H}, D={D}")
+        for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
+            if t.dtype != torch.float32 or tuple(t.shape) != (N, D // 2) or not t.is_contiguous() or t.device != cpu:
+                raise ValueError(f"{name} must be a contiguous float32 [{N}, {D // 2}] host tensor")
+        if out is None:
+            out = torch.empty(q.shape, dtype=out_dtype, pin_memory=True)
+        elif out.shape != q.shape or not out.is_contiguous() or out.device != cpu:
+            raise ValueError("out must be a contiguous [1, H, N, D] host tensor")
+        st = lib.lin_attn_forward_fused_host(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), rope_cos.data_ptr(),
+                                             rope_sin.data_ptr(), out.data_ptr(), _out_code(out.dtype), N,
+                                             _mode(mode), _stream_handle(stream, self.device))
+        _check(st, "lin_attn_forward_fused_host")
         return out
 
     def debug_kv(self, stream=None):
