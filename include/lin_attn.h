@@ -32,7 +32,11 @@
  *   - The caller owns every tensor; the context owns only its scratch.
  *   - Calls enqueue on `stream` (a cudaStream_t; NULL = legacy default stream) and return
  *     without synchronising, unless stated otherwise.
- *   - A context may be used by one stream at a time (its scratch is shared by all calls).
+ *   - The layer calls (lin_attn_forward, _layout, _fused, _fused_layout) enqueue kernel
+ *     launches only - no allocation, no synchronisation - so a sequence of them may be
+ *     captured into a CUDA graph (stream capture); the replay gives the same bits.
+ *   - A context may be used by one stream at a time (its scratch is shared by all calls);
+ *     distinct contexts share no device state and may run at once.
  *   - `out` must not overlap any input.
  *   - Return value: LIN_ATTN_OK or one of the LIN_ATTN_ERR_* codes below; on error nothing
  *     was enqueued (except LIN_ATTN_ERR_CUDA after a failed launch) and
